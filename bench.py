@@ -1,0 +1,391 @@
+#!/usr/bin/env python3
+"""Benchmark of volumetric delay-and-sum on GB300: DAS accumulations/s.
+
+One step = one das_beamform call over the whole workload (RF permute + DAS
+kernel), inputs resident in HBM.  Default workload: the 32 x 32 matrix-array
+volume (M = 1024 receivers, Q = 9 diverging waves, K = 2048 float32 samples,
+64^3 voxels, B = 32 frames) -- 7.73e10 accumulations per step.  Its 2.4 GB RF
+record is far larger than the 129 MB L2, so no explicit L2 flush is needed.
+
+Prints ONE JSON line (rank 0).  Besides the device-timed value it reports:
+  roofline      the DAS kernel against the FP32 issue roofline (alu bound);
+  cpu_baseline  the float64 oracle on the host cores, on a bounded voxel sample;
+  e2e           the same metric through das_beamform_host with pinned host
+                buffers (host->device and device->host copies inside the timing);
+  clocks        SM clocks and throttle reasons sampled during the timed region.
+
+``--impl reference`` times the oracle itself (the reference arm: a plain CPU
+program) on bounded samples of the same workload.  Under torchrun with N > 1
+GPUs every rank runs an independent replica (weak scaling, no collective on the
+data path); the timing takes the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DAS accumulations/s (B·N·Q·M/time) at 1 GB300; fraction of roofline"
+UNIT = "accumulations/s"
+ISSUE_SLOTS_PER_ACC = 5        # ~2 loads + 3 FMA per accumulation at FP32 issue peak
+FP32_LANES_PER_SM = 128
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="full", choices=["tiny", "mid", "full", "iq", "large"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "bl", "bi", "brick"])
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def describe(wl) -> str:
+    tx = {"dw": f"{wl.Q} diverging waves", "pw": f"{wl.Q} plane waves"}[wl.transmit]
+    dt = "c64 IQ" if wl.iq else "f32 RF"
+    return (f"{wl.name}: {wl.n_el}x{wl.n_el} array (M={wl.M}), {tx}, K={wl.K} {dt} at "
+            f"{wl.fs / 1e6:g} MHz, {wl.nx}x{wl.ny}x{wl.nz} voxels (N={wl.N}), B={wl.B}, F#={wl.fnum}")
+
+
+def aperture_pairs(prob) -> int:
+    """Number of (voxel, receiver) pairs inside the F-number aperture."""
+    nx, ny, nz, x0, y0, z0, dx, dy, dz = prob.grid
+    xs = x0 + np.arange(nx) * dx
+    ys = y0 + np.arange(ny) * dy
+    rx = prob.rx.astype(np.float64)
+    two_f2 = (2.0 * prob.fnum) ** 2
+    ddx = (xs[:, None] - rx[None, :, 0]) ** 2          # nx x M
+    ddy = (ys[:, None] - rx[None, :, 1]) ** 2          # ny x M
+    total = 0
+    for iz in range(nz):
+        ez = z0 + iz * dz - rx[:, 2]                    # M
+        lim = np.where(ez > 0, ez * ez / two_f2, -1.0)  # rho^2 limit per receiver
+        for m0 in range(0, rx.shape[0], 256):
+            sl = slice(m0, m0 + 256)
+            inside = (ddx[:, None, sl] + ddy[None, :, sl]) <= lim[None, None, sl]
+            total += int(inside.sum())
+    return total
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(float(r[2]) for r in rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit()),
+                "samples": len(rows), "reasons": reasons}
+
+
+# ------------------------------------------------------------ CPU oracle
+def time_oracle(prob, target_s: float, seed: int):
+    """Oracle accumulations/s on a seeded voxel sample sized to ~target_s."""
+    import oracle
+    orc = oracle.load()
+    cores = os.cpu_count() or 1
+    per_voxel = prob.B * prob.Q * prob.M
+    g = oracle.Grid(*prob.grid)
+    kw = dict(c=prob.c, fs=prob.fs, t0=prob.t0, fnum=prob.fnum, f_demod=prob.f_demod,
+              nthreads=cores)
+    probe = synth_sample(prob.N, min(prob.N, 4 * cores), seed)
+    t = time.perf_counter()
+    orc.beamform(prob.rf, prob.tau_tx, prob.w_tx, prob.rx.astype(np.float64), g, idx=probe, **kw)
+    rate = len(probe) / max(time.perf_counter() - t, 1e-6)
+    count = int(min(prob.N, max(len(probe), rate * target_s)))
+    idx = synth_sample(prob.N, count, seed + 1)
+    t = time.perf_counter()
+    orc.beamform(prob.rf, prob.tau_tx, prob.w_tx, prob.rx.astype(np.float64), g, idx=idx, **kw)
+    dt = time.perf_counter() - t
+    return {"value": count * per_voxel / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{count} seeded voxels of {prob.N} (all B, Q, M); {dt:.1f} s",
+            "seconds": dt}
+
+
+def synth_sample(N, count, seed):
+    from volumetric_ultrasound_delay_gb300 import synth
+    return synth.sample_voxels(N, count, seed)
+
+
+# --------------------------------------------------------- distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value: float) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def source_sha(kernel: str) -> str:
+    name = {"brick": "das_brick.cu", "bi": "das_bi.cu", "bl": "das_bl.cu"}[kernel]
+    h = hashlib.sha256()
+    for f in (name, "das_device.cuh", "das_internal.cuh"):
+        with open(os.path.join(ROOT, "volumetric_ultrasound_delay_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    key = f"{kernel}/{workload}"
+    r = rec.get(key)
+    if not r or r.get("source_sha") != source_sha(kernel):
+        return None   # never measured, or the kernel changed since the counters were taken
+    return r.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------- arms
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    from volumetric_ultrasound_delay_gb300 import synth
+    import oracle
+    oracle.build()
+    prob = synth.make_problem(args.workload)
+    cores = os.cpu_count() or 1
+    per_step = max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
+    # size one step's voxel sample from a probe run
+    cal = time_oracle(prob, per_step, seed=100)
+    count = min(prob.N, max(1, int(cal["value"] * per_step / (prob.B * prob.Q * prob.M))))
+    import oracle as om
+    orc = om.load()
+    g = om.Grid(*prob.grid)
+    kw = dict(c=prob.c, fs=prob.fs, t0=prob.t0, fnum=prob.fnum, f_demod=prob.f_demod, nthreads=cores)
+    rx64 = prob.rx.astype(np.float64)
+    times = []
+    for s in range(args.warmup + args.steps):
+        idx = synth.sample_voxels(prob.N, count, 1000 + s)
+        t = time.perf_counter()
+        orc.beamform(prob.rf, prob.tau_tx, prob.w_tx, rx64, g, idx=idx, **kw)
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t)
+    acc = count * prob.B * prob.Q * prob.M
+    value = acc * len(times) / sum(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded numpy: noise + point-scatterer echoes)",
+        "config": {"workload": describe(prob.wl), "sample_per_step": f"{count} seeded voxels"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{count} seeded voxels of {prob.N} per step (all B, Q, M)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    from volumetric_ultrasound_delay_gb300 import das, synth
+    from volumetric_ultrasound_delay_gb300 import build as libbuild
+    libbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    prob = synth.make_problem(args.workload)
+    dtype = "c64" if prob.wl.iq else "f32"
+    A = prob.B * prob.N * prob.Q * prob.M
+    rf = torch.from_numpy(prob.rf).to(dev)
+    tau = torch.from_numpy(prob.tau_tx).to(dev)
+    w = torch.from_numpy(prob.w_tx).to(dev)
+    out = torch.empty((prob.B, prob.N), dtype=torch.complex64 if prob.wl.iq else torch.float32,
+                      device=dev)
+    plan = das.Plan(prob.grid, prob.rx, prob.c, prob.fs, prob.t0, prob.fnum, dtype, prob.B,
+                    prob.Q, prob.M, prob.K, kernel=args.kernel, f_demod=prob.f_demod)
+    kernel = plan.kernel
+    plan.set_option(das.OPT_TIMING, 1)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(max(3, args.warmup)):
+        plan.beamform(rf, tau, w, out, stream=stream)
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    das_ms, perm_ms = [], []
+    ev0.record(stream)
+    for _ in range(args.steps):
+        plan.beamform(rf, tau, w, out, stream=stream)
+        p_ms, d_ms = plan.last_times()      # events recorded by the library on `stream`
+        perm_ms.append(p_ms)
+        das_ms.append(d_ms)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    elapsed_ms = max_over_ranks(world, ev0.elapsed_time(ev1))
+    ms_per_step = elapsed_ms / args.steps
+    value = world * A / (ms_per_step / 1e3)
+
+    # ---------------- e2e through the host entry point (pinned buffers)
+    e2e = None
+    if not args.no_e2e:
+        rf_h = torch.from_numpy(prob.rf).pin_memory()
+        tau_h = torch.from_numpy(prob.tau_tx).pin_memory()
+        w_h = torch.from_numpy(prob.w_tx).pin_memory()
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        plan.beamform_host(rf_h, tau_h, w_h, out_h, stream=stream)      # warm-up, allocates
+        barrier(world)
+        t = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            plan.beamform_host(rf_h, tau_h, w_h, out_h, stream=stream)
+        e2e_s = max_over_ranks(world, (time.perf_counter() - t) / args.e2e_steps)
+        e2e = {"value": world * A / e2e_s, "unit": UNIT,
+               "h2d_bytes_per_step": int(rf_h.numel() * rf_h.element_size() + 2 * tau_h.numel() * 4),
+               "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size()),
+               "ms_per_step": 1e3 * e2e_s}
+        if not torch.equal(out_h, out.cpu()):
+            raise RuntimeError("host entry point disagrees with the device entry point")
+
+    # ---------------- roofline of the dominant kernel (the DAS kernel)
+    pairs = aperture_pairs(prob)
+    a_eff = prob.B * prob.Q * pairs
+    props = torch.cuda.get_device_properties(dev)
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+        sm_max = float(peaks["sm_max_mhz"])
+        peak_src = "MEASURED_PEAKS.json sm_max_mhz"
+    except (OSError, ValueError, KeyError):
+        sm_max = 2070.0
+        peak_src = "nominal max SM clock"
+    peak = props.multi_processor_count * FP32_LANES_PER_SM * sm_max * 1e6 / 1e12   # T issue/s
+    das_mean = statistics.mean(das_ms)
+    achieved = ISSUE_SLOTS_PER_ACC * a_eff / (das_mean / 1e3) / 1e12
+    traffic = measured_traffic(kernel, args.workload)
+    roofline = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tinst/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "kernel": f"das_{kernel}_kernel", "kernel_ms": das_mean,
+                "work": f"{ISSUE_SLOTS_PER_ACC} FP32 issue slots x {a_eff:.4g} in-aperture "
+                        f"accumulations per launch ({pairs / (prob.N * prob.M):.3f} of B*N*Q*M)",
+                "peak_source": f"{props.multi_processor_count} SMs x {FP32_LANES_PER_SM} lanes x "
+                               f"{sm_max:g} MHz ({peak_src})"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = time_oracle(prob, args.cpu_seconds, seed=7)
+        cpu.pop("seconds", None)
+
+    launches = args.steps * (1 if kernel == "bl" else 2)
+    plan.close()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "c64" if prob.wl.iq else "f32",
+        "data": "synthetic (seeded numpy: N(0,1) noise + point-scatterer echoes)",
+        "config": {"workload": describe(prob.wl), "kernel": kernel,
+                   "accumulations_per_step": A,
+                   "in_aperture_fraction": pairs / (prob.N * prob.M),
+                   "l2": f"inputs larger than L2 ({prob.rf.nbytes / 1e9:.2f} GB RF record), no flush",
+                   "replicas": world},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": launches,
+        "kernel_ms": {"permute": statistics.mean(perm_ms), "das": das_mean},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

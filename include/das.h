@@ -1,0 +1,188 @@
+/*
+ * das.h -- C ABI of libdas, volumetric delay-and-sum (DAS) beamforming on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation (ffdas paper, "ffdas: volumetric ultrasound reconstruction at
+ * warp speed", Methods, the accumulation it numbers Eq. (2); ffdas docs, "How
+ * It Works", section "The computational challenge"):
+ *
+ *   y[b,n] = sum_q sum_m  w_tx[q,n] * w_rx[m,n] * P_qmn * S_bqm(f_qmn)
+ *   f_qmn  = (tau_tx[q,n] + |x_n - r_m| / c - t0) * fs
+ *   S(f)   = (1 - a) s[k0] + a s[k0+1],  k0 = floor(f), a = f - k0,
+ *            with every sample outside [0, K-1] counting as zero
+ *   w_rx   = 1 if dz > 0 and 2 F# rho <= dz else 0  (rho: lateral distance,
+ *            dz: depth of the voxel below the receiver; F# <= 0: w_rx = 1)
+ *   P_qmn  = exp(+i 2 pi f_demod (tau_tx[q,n] + |x_n - r_m| / c)) for complex
+ *            (IQ) records, 1 for real records
+ *
+ * Transmit delays and weights are inputs per (q, n); receive delays and the
+ * aperture weight are computed inside the kernels from the geometry, never
+ * from a stored delay table (ffdas paper, Methods, first paragraph; ffdas
+ * docs, "The computational challenge").
+ *
+ * Conventions for every call:
+ *  - Device pointers are CUDA device (or managed) memory of the current
+ *    device, C-contiguous, and 16-byte aligned; host pointers are ordinary
+ *    host memory (page-locked memory makes the host entry point faster).
+ *  - The caller owns every buffer it passes in; the library never frees them.
+ *  - A call validates its arguments on the host first.  A rejected call
+ *    returns an error code, launches nothing and leaves outputs untouched.
+ *  - Device work is asynchronous on the given stream unless stated
+ *    otherwise; the caller synchronises before reading results.
+ *  - No kernel traps, asserts or waits without a bound.
+ *  - das_last_error_string() describes the last error of the calling thread.
+ */
+#ifndef DAS_H
+#define DAS_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct das_plan_s *das_plan;
+
+typedef enum {
+    DAS_OK = 0,
+    DAS_ERR_INVALID_ARG = 1,    /* null pointer, bad size, misaligned buffer ... */
+    DAS_ERR_UNSUPPORTED = 2,    /* valid request this kernel/dtype cannot serve */
+    DAS_ERR_OUT_OF_MEMORY = 3,  /* device or host allocation failed */
+    DAS_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
+    DAS_ERR_TIMEOUT = 5         /* reserved: a bounded device wait ran out */
+} das_status;
+
+/* Sample type of the RF record and of the output. */
+typedef enum {
+    DAS_F32 = 0,   /* real float32 RF -> real float32 y */
+    DAS_C64 = 1    /* interleaved complex64 IQ -> complex64 y */
+} das_dtype;
+
+/* Kernel choice (das_plan_set_option(DAS_OPT_KERNEL, ...)). */
+typedef enum {
+    DAS_KERNEL_AUTO = 0,   /* brick kernel when it supports the plan, else BI, else BL */
+    DAS_KERNEL_BL = 1,     /* per-voxel baseline on the native B x Q x M x K record
+                              (ffdas paper, Methods, baseline paragraph / Algorithm 1;
+                              ffdas docs, ALG1) */
+    DAS_KERNEL_BI = 2,     /* batch-inner warp tiling on a K x Q x M x B copy
+                              (ffdas paper, Methods, batch-inner paragraphs /
+                              Algorithm 2; ffdas docs, ALG2) */
+    DAS_KERNEL_BRICK = 3   /* this library's sm_103a design: voxel bricks per CTA,
+                              per-(voxel, transmit, receiver) geometry staged in
+                              shared memory, receivers outside every aperture of
+                              the brick skipped, Q x M x K x B copy */
+} das_kernel;
+
+/* Plan options. */
+typedef enum {
+    DAS_OPT_KERNEL = 0,    /* das_kernel value */
+    DAS_OPT_DEMOD_HZ = 1,  /* f_demod in Hz for DAS_C64 plans (default 0: no rotation);
+                              non-zero on a DAS_F32 plan is DAS_ERR_UNSUPPORTED */
+    DAS_OPT_TIMING = 2,    /* 1: record CUDA events around the permute and the DAS
+                              kernel of each das_beamform (read them with
+                              das_plan_last_times); 0 (default): no events */
+    DAS_OPT_BI_GROUP = 3   /* BI kernel: lanes per voxel G in {2,4,8,16,32}; 0 = automatic */
+} das_option;
+
+/* Regular voxel grid: voxel n = ix + nx*(iy + ny*iz) sits at
+ * (x0 + ix*dx, y0 + iy*dy, z0 + iz*dz), metres.  The receivers face +z. */
+typedef struct {
+    int nx, ny, nz;
+    float x0, y0, z0;
+    float dx, dy, dz;
+} das_grid;
+
+/*
+ * Creates a plan for fixed geometry and sizes (ffdas paper, Methods: geometry
+ * on the fly; the call follows the problem statement of the method).
+ *   grid     host, regular voxel grid (N = nx*ny*nz voxels), copied.
+ *   rx_xyz   host, M x 3 float32 receiver positions (metres), copied.
+ *   c, fs    speed of sound (m/s) and sampling rate (Hz), both > 0.
+ *   t0       time of sample 0 (seconds).
+ *   fnum     receive F-number; <= 0 disables the aperture.
+ *   dtype    DAS_F32 or DAS_C64.
+ *   B,Q,M,K  frames, transmits, receivers, samples per record (all >= 1);
+ *            Q*M*K and B*N must stay below 2^31, K below 2^22.
+ * Allocates the device copies of the geometry; the permute scratch of the BI
+ * and brick kernels (B*Q*M*K elements) is allocated on first use.
+ * Errors: DAS_ERR_INVALID_ARG, DAS_ERR_OUT_OF_MEMORY, DAS_ERR_CUDA; *plan is
+ * set to NULL on failure.  The plan belongs to the device current at creation.
+ */
+das_status das_plan_create(das_plan *plan, const das_grid *grid, const float *rx_xyz,
+                           float c, float fs, float t0, float fnum, das_dtype dtype,
+                           int B, int Q, int M, int K);
+
+/* Sets / reads one das_option.  Errors: DAS_ERR_INVALID_ARG (null plan, unknown
+ * option or value), DAS_ERR_UNSUPPORTED (see DAS_OPT_DEMOD_HZ). */
+das_status das_plan_set_option(das_plan plan, int option, double value);
+das_status das_plan_get_option(das_plan plan, int option, double *value);
+
+/* The kernel das_beamform will run for this plan (after AUTO resolution). */
+das_status das_plan_kernel(das_plan plan, int *kernel);
+
+/*
+ * y = DAS(rf) on the device (the formula at the top of this file).
+ *   rf       device, B x Q x M x K, k contiguous (float32, or interleaved
+ *            complex64 for DAS_C64).
+ *   tau_tx   device, Q x N float32 transmit delays (seconds).
+ *   w_tx     device, Q x N float32 transmit weights.
+ *   out      device, B x N (float32 or complex64); fully overwritten.
+ *   stream   CUDA stream of the plan's device (0 = legacy default stream).
+ * The BI and brick kernels first permute rf into the plan's scratch (ffdas
+ * paper, Methods, batch-inner paragraph; ffdas docs, ALG2: permuted as part of
+ * the launch), so one plan must not run two das_beamform calls at once; use one
+ * plan per concurrent stream.
+ * Errors: DAS_ERR_INVALID_ARG (null or misaligned pointers), DAS_ERR_UNSUPPORTED
+ * (kernel cannot serve this plan), DAS_ERR_OUT_OF_MEMORY (scratch), DAS_ERR_CUDA
+ * (launch failure).  Asynchronous.
+ */
+das_status das_beamform(das_plan plan, const void *rf, const float *tau_tx,
+                        const float *w_tx, void *out, cudaStream_t stream);
+
+/*
+ * The same computation from host buffers (same layouts as das_beamform, host
+ * memory): copies the inputs to plan-owned device buffers on `stream`, runs
+ * das_beamform, copies y back and synchronises the stream before returning.
+ * Device buffers (about the size of rf) are allocated on first use and kept.
+ * Errors: as das_beamform.  Synchronous.
+ */
+das_status das_beamform_host(das_plan plan, const void *rf_host, const float *tau_tx_host,
+                             const float *w_tx_host, void *out_host, cudaStream_t stream);
+
+/* Device milliseconds of the permute and of the DAS kernel of the last
+ * das_beamform on this plan, when DAS_OPT_TIMING is 1 (synchronises on the
+ * recorded events).  permute_ms is 0 for the BL kernel.  Errors:
+ * DAS_ERR_INVALID_ARG when timing is off or no call was made yet. */
+das_status das_plan_last_times(das_plan plan, float *permute_ms, float *das_ms);
+
+/* Bytes of device memory the plan holds now. */
+das_status das_plan_device_bytes(das_plan plan, size_t *bytes);
+
+/* Frees everything the plan owns (synchronous; waits for its device work).
+ * A NULL plan is a no-op returning DAS_OK. */
+das_status das_plan_destroy(das_plan plan);
+
+/*
+ * RF layout permute (ffdas paper, Methods, batch-inner paragraph: B x Q x M x K
+ * with k contiguous -> a layout with b contiguous).  A bit-exact copy.
+ *   layout 0: K x Q x M x B (the pages' batch-inner layout)
+ *   layout 1: Q x M x K x B (rows of one (q, m) adjacent; used by the brick kernel)
+ *   in, out  device buffers of B*Q*M*K elements of dtype, not overlapping.
+ * Errors: DAS_ERR_INVALID_ARG, DAS_ERR_CUDA.  Asynchronous.
+ */
+das_status das_permute(const void *in, void *out, das_dtype dtype, int B, int Q, int M,
+                       int K, int layout, cudaStream_t stream);
+
+/* Text of the last error raised on the calling thread ("" if none). */
+const char *das_last_error_string(void);
+
+/* Library version, e.g. "1.0.0". */
+const char *das_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DAS_H */

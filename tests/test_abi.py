@@ -1,0 +1,67 @@
+"""The C-ABI library builds, loads without a GPU, exports every declared symbol,
+and rejects invalid calls on the host (no device work is requested here)."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+from volumetric_ultrasound_delay_gb300 import build as build_mod
+
+HEADER = Path(__file__).resolve().parent.parent / "include" / "das.h"
+
+
+@pytest.fixture(scope="module")
+def libdas():
+    build_mod.build()
+    from volumetric_ultrasound_delay_gb300 import das
+    return das.lib()
+
+
+def declared_functions():
+    text = re.sub(r"/\*.*?\*/", "", HEADER.read_text(), flags=re.S)
+    return sorted(set(re.findall(r"\b(das_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("das_plan_create", "das_beamform", "das_plan_destroy", "das_permute"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(libdas):
+    for name in declared_functions():
+        assert hasattr(libdas, name), name
+
+
+def test_binding_covers_every_symbol():
+    from volumetric_ultrasound_delay_gb300 import das
+    assert sorted(das._SIGS) == declared_functions()
+
+
+def test_host_side_rejections(libdas):
+    from volumetric_ultrasound_delay_gb300 import das
+    h = ctypes.c_void_p()
+    g = das._Grid(4, 4, 4, 0.0, 0.0, 0.01, 1e-3, 1e-3, 1e-3)
+    rx = (ctypes.c_float * 3)(0.0, 0.0, 0.0)
+    # null plan pointer, null grid, bad sizes, bad physics: all rejected before any CUDA call
+    assert libdas.das_plan_create(None, ctypes.byref(g), rx, 1540.0, 20e6, 0.0, 1.5, 0, 1, 1, 1, 8) == das.DAS_ERR_INVALID_ARG
+    assert libdas.das_plan_create(ctypes.byref(h), None, rx, 1540.0, 20e6, 0.0, 1.5, 0, 1, 1, 1, 8) == das.DAS_ERR_INVALID_ARG
+    assert libdas.das_plan_create(ctypes.byref(h), ctypes.byref(g), rx, 1540.0, 20e6, 0.0, 1.5, 0, 0, 1, 1, 8) == das.DAS_ERR_INVALID_ARG
+    assert libdas.das_plan_create(ctypes.byref(h), ctypes.byref(g), rx, -1.0, 20e6, 0.0, 1.5, 0, 1, 1, 1, 8) == das.DAS_ERR_INVALID_ARG
+    assert libdas.das_plan_create(ctypes.byref(h), ctypes.byref(g), rx, 1540.0, 20e6, 0.0, 1.5, 7, 1, 1, 1, 8) == das.DAS_ERR_INVALID_ARG
+    assert libdas.das_plan_create(ctypes.byref(h), ctypes.byref(g), rx, 1540.0, 20e6, 0.0, 1.5, 0, 1, 1, 1, 1 << 22) == das.DAS_ERR_INVALID_ARG
+    assert h.value is None
+    assert b"K must be" in libdas.das_last_error_string()
+    bad = das._Grid(0, 4, 4, 0.0, 0.0, 0.01, 1e-3, 1e-3, 1e-3)
+    assert libdas.das_plan_create(ctypes.byref(h), ctypes.byref(bad), rx, 1540.0, 20e6, 0.0, 1.5, 0, 1, 1, 1, 8) == das.DAS_ERR_INVALID_ARG
+    # calls on a NULL plan
+    assert libdas.das_beamform(None, None, None, None, None, None) == das.DAS_ERR_INVALID_ARG
+    assert libdas.das_plan_set_option(None, 0, 0.0) == das.DAS_ERR_INVALID_ARG
+    assert libdas.das_plan_destroy(None) == das.DAS_OK
+    # permute argument checks
+    assert libdas.das_permute(None, None, 0, 1, 1, 1, 1, 0, None) == das.DAS_ERR_INVALID_ARG
+    buf = ctypes.create_string_buffer(64)
+    assert libdas.das_permute(buf, buf, 0, 1, 1, 1, 4, 0, None) == das.DAS_ERR_INVALID_ARG  # overlap
+    assert libdas.das_permute(buf, ctypes.byref(buf, 32), 0, 1, 1, 1, 4, 2, None) == das.DAS_ERR_INVALID_ARG
+    assert libdas.das_version() == b"1.0.0"

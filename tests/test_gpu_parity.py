@@ -1,0 +1,229 @@
+"""GPU parity: every kernel through the C ABI against the float64 oracle.
+
+Bars: the permute is bit-exact; beamformed output satisfies
+max(|y_gpu - y_oracle| - slack) <= 1e-4 * max|y_oracle| (slack: aperture-tie
+pairs the oracle flags, usually none).  Small cases are compared element by
+element on every voxel; the full-size workloads run in the bench's launch
+configuration and are compared on seeded voxel samples.
+"""
+import zlib
+
+import numpy as np
+import pytest
+
+from parity import TOL, device_inputs, error_ratio, gpu_beamform, oracle_beamform, plan_for
+from volumetric_ultrasound_delay_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # pragma: no cover - CPU containers skip these
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+KERNELS = ["bl", "bi", "brick"]
+
+# Workloads shrunk (8x8 array, small ragged grids) so the oracle finishes in a
+# second or two; B, Q, K, dtype and transmit geometry are those of each workload.
+SMALL = {
+    "tiny": dict(),
+    "mid_s": dict(base="mid", n_el=8, nx=17, ny=9, nz=6),
+    "full_s": dict(base="full", n_el=8, nx=19, ny=13, nz=5),
+    "iq_s": dict(base="iq", n_el=8, nx=11, ny=9, nz=4),
+    "large_s": dict(base="large", n_el=8, nx=13, ny=11, nz=3),
+}
+
+
+def small_problem(name):
+    kw = dict(SMALL[name])
+    base = kw.pop("base", name)
+    return synth.make_problem(base, **kw)
+
+
+@pytest.fixture(scope="module")
+def small_problems():
+    return {k: small_problem(k) for k in SMALL}
+
+
+# ------------------------------------------------------------------ permute
+@pytest.mark.parametrize("shape", [(32, 9, 16, 2048), (16, 3, 7, 100), (3, 2, 5, 37),
+                                   (1, 1, 1, 1), (5, 1, 3, 64), (40, 2, 3, 33)])
+@pytest.mark.parametrize("dtype", ["f32", "c64"])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_permute_bit_exact(oracle, shape, dtype, layout):
+    from volumetric_ultrasound_delay_gb300 import das
+    rng = np.random.default_rng(zlib.crc32(repr((shape, dtype, layout)).encode()))
+    if dtype == "c64":
+        x = (rng.standard_normal(shape) + 1j * rng.standard_normal(shape)).astype(np.complex64)
+    else:
+        x = rng.standard_normal(shape).astype(np.float32)
+    src = torch.from_numpy(x).cuda()
+    dst = torch.empty_like(src).reshape(-1)
+    das.permute(src, dst, layout)
+    torch.cuda.synchronize()
+    want = oracle.permute(x, "kqmb" if layout == 0 else "qmkb")
+    assert dst.cpu().numpy().tobytes() == want.tobytes()
+
+
+# ------------------------------------------------- small workloads, all voxels
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_workload_all_voxels(oracle, small_problems, name, kernel):
+    prob = small_problems[name]
+    y, used = gpu_beamform(prob, kernel)
+    assert used == kernel
+    ref, slack = oracle_beamform(oracle, prob)
+    ratio = error_ratio(y, ref, slack)
+    assert ratio <= TOL, (name, kernel, ratio)
+
+
+def test_auto_picks_brick_and_kernels_agree(small_problems):
+    prob = small_problems["full_s"]
+    outs = {k: gpu_beamform(prob, k)[0] for k in KERNELS}
+    y_auto, used = gpu_beamform(prob, "auto")
+    assert used == "brick"
+    assert np.array_equal(y_auto, outs["brick"])
+    peak = np.abs(outs["bl"]).max()
+    for k in ("bi", "brick"):
+        assert np.abs(outs[k] - outs["bl"]).max() <= TOL * peak
+
+
+# ------------------------------------------------------------- edge cases
+def _custom(**kw):
+    base = dict(n_el=4, nx=5, ny=3, nz=2, B=8, K=64, n_scat=2, z_range=(2e-3, 4e-3))
+    base.update(kw)
+    return synth.make_problem(synth.workload("tiny", **base))
+
+
+EDGE = {
+    "B1": dict(B=1),
+    "B3": dict(B=3),
+    "B8": dict(B=8),
+    "B4": dict(B=4),
+    "K2": dict(K=2),
+    "K3": dict(K=3),
+    "M1": dict(n_el=1),
+    "Q1": dict(angles_x_deg=(5.0,)),
+    "N1": dict(nx=1, ny=1, nz=1),
+    "past_record": dict(K=20),                       # most delays beyond the record
+    "no_aperture": dict(fnum=0.0),
+    "t0_shift": dict(t0=1.5e-6),
+    "iq_B2": dict(iq=True, fs=10e6, f_demod=5e6, B=2, K=128),
+    "iq_B6": dict(iq=True, fs=10e6, f_demod=5e6, B=6, K=128),
+    "iq_B16": dict(iq=True, fs=10e6, f_demod=5e6, B=16, K=128),
+    "iq_B32": dict(iq=True, fs=10e6, f_demod=5e6, B=32, K=128),
+    "f32_B64": dict(B=64, K=96),
+    "f32_B128": dict(B=128, K=64),
+}
+
+
+@pytest.mark.parametrize("name", list(EDGE))
+def test_edge_cases(oracle, name):
+    prob = _custom(**EDGE[name])
+    ref, slack = oracle_beamform(oracle, prob)
+    from volumetric_ultrasound_delay_gb300 import das
+    for kernel in ["auto"] + KERNELS:
+        try:
+            y, _ = gpu_beamform(prob, kernel)
+        except das.DasError as exc:
+            assert exc.status == das.DAS_ERR_UNSUPPORTED and kernel in ("bi", "brick"), (name, kernel)
+            continue
+        assert error_ratio(y, ref, slack) <= TOL, (name, kernel, error_ratio(y, ref, slack))
+
+
+def test_nan_delay_contributes_nothing(oracle):
+    prob = _custom(B=8)
+    prob.tau_tx[1, 3] = np.nan
+    prob.tau_tx[0, 5] = np.inf
+    ref, slack = oracle_beamform(oracle, prob)
+    for kernel in KERNELS:
+        y, _ = gpu_beamform(prob, kernel)
+        assert np.all(np.isfinite(y))
+        assert error_ratio(y, ref, slack) <= TOL, kernel
+
+
+def test_all_outside_aperture_is_zero():
+    # voxels above the array (dz < 0): no receiver is inside any aperture
+    prob = _custom(z_range=(-4e-3, -2e-3))
+    for kernel in KERNELS:
+        y, _ = gpu_beamform(prob, kernel)
+        assert not np.any(y), kernel
+
+
+def test_unsupported_requests_are_rejected():
+    from volumetric_ultrasound_delay_gb300 import das
+    prob = _custom(B=3)
+    for kernel in ("bi", "brick"):
+        with pytest.raises(das.DasError) as exc:
+            gpu_beamform(prob, kernel)
+        assert exc.value.status == das.DAS_ERR_UNSUPPORTED
+    plan = plan_for(prob)
+    with pytest.raises(das.DasError):
+        plan.set_option(das.OPT_DEMOD_HZ, 5e6)   # real plan cannot demodulate
+    plan.close()
+
+
+def test_misaligned_and_wrong_sizes_rejected():
+    from volumetric_ultrasound_delay_gb300 import das
+    prob = _custom(B=8)
+    plan = plan_for(prob)
+    rf, tau, w = device_inputs(prob)
+    out = torch.empty((prob.B, prob.N), dtype=torch.float32, device="cuda")
+    with pytest.raises(ValueError):
+        plan.beamform(rf[:, :, :, :-1].contiguous(), tau, w, out)
+    flat = torch.empty(rf.numel() + 1, dtype=torch.float32, device="cuda")
+    mis = flat[1:]
+    mis.copy_(rf.reshape(-1))
+    h = das.lib().das_beamform(plan._h, mis.data_ptr(), tau.data_ptr(), w.data_ptr(),
+                               out.data_ptr(), None)
+    assert h == das.DAS_ERR_INVALID_ARG
+    plan.close()
+
+
+def test_host_entry_point_matches_device(small_problems):
+    prob = small_problems["full_s"]
+    y_dev, _ = gpu_beamform(prob)
+    plan = plan_for(prob)
+    out = np.empty((prob.B, prob.N), dtype=np.float32)
+    plan.beamform_host(np.ascontiguousarray(prob.rf), prob.tau_tx, prob.w_tx, out)
+    plan.close()
+    assert np.array_equal(out, y_dev)
+
+
+def test_timing_option_reports_both_kernels(small_problems):
+    from volumetric_ultrasound_delay_gb300 import das
+    prob = small_problems["full_s"]
+    plan = plan_for(prob)
+    plan.set_option(das.OPT_TIMING, 1)
+    plan.beamform(*device_inputs(prob))
+    perm_ms, das_ms = plan.last_times()
+    assert perm_ms > 0 and das_ms > 0
+    plan.close()
+
+
+def test_repeated_calls_are_deterministic(small_problems):
+    prob = small_problems["iq_s"]
+    inputs = device_inputs(prob)
+    a, _ = gpu_beamform(prob, inputs=inputs)
+    b, _ = gpu_beamform(prob, inputs=inputs)
+    assert np.array_equal(a, b)
+
+
+# --------------------------------------- full-size workloads, sampled voxels
+FULL = [("mid", 1024), ("full", 1024), ("iq", 512), ("large", 4096)]
+
+
+@pytest.mark.parametrize("name,samples", FULL)
+def test_full_size_sampled(oracle, name, samples):
+    prob = synth.make_problem(name)
+    inputs = device_inputs(prob)
+    idx = synth.sample_voxels(prob.N, samples, seed=prob.wl.seed)
+    ref, slack = oracle_beamform(oracle, prob, idx=idx)
+    kernels = ["auto", "bi"] + (["bl"] if name in ("mid", "full") else [])
+    for kernel in kernels:
+        y, used = gpu_beamform(prob, kernel, inputs=inputs)
+        ratio = error_ratio(y[:, idx], ref, slack)
+        assert ratio <= TOL, (name, used, ratio)
+        # every output is finite and the volume is not empty
+        assert np.all(np.isfinite(y)) and np.abs(y).max() > 0
+    del inputs
+    torch.cuda.empty_cache()

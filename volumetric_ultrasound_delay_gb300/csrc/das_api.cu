@@ -1,0 +1,399 @@
+// C ABI of libdas: plan management, argument checks and kernel dispatch.
+// Every entry point validates on the host, launches nothing when it rejects a
+// call, and maps CUDA failures to DAS_ERR_CUDA with a readable message.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "das_internal.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+das_status fail(das_status st, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+das_status cuda_fail(cudaError_t e, const char *what)
+{
+    if (e == cudaErrorMemoryAllocation)
+        return fail(DAS_ERR_OUT_OF_MEMORY, "%s: %s", what, cudaGetErrorString(e));
+    return fail(DAS_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+struct das_plan_s {
+    das_grid grid{};
+    float c = 0, fs = 0, t0 = 0, fnum = 0;
+    das_dtype dtype = DAS_F32;
+    int B = 0, Q = 0, M = 0, K = 0;
+    long long N = 0;
+    int device = 0;
+    int num_sms = 1;
+    int kernel = DAS_KERNEL_AUTO;
+    int bi_group = 0;
+    double f_demod = 0.0;
+    int timing = 0;
+    bool timed_once = false;
+    bool last_had_permute = false;
+    cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+    RxPos *d_rx = nullptr;
+    void *d_perm = nullptr;
+    size_t perm_bytes = 0;
+    // device staging of das_beamform_host
+    void *d_rf = nullptr, *d_out = nullptr;
+    float *d_tau = nullptr, *d_w = nullptr;
+    DasGeom geom{};
+
+    size_t elem_bytes() const { return dtype == DAS_C64 ? 8 : 4; }
+    size_t rf_bytes() const { return (size_t)B * Q * M * K * elem_bytes(); }
+    size_t out_bytes() const { return (size_t)B * (size_t)N * elem_bytes(); }
+    size_t txw_bytes() const { return (size_t)Q * (size_t)N * sizeof(float); }
+};
+
+namespace {
+
+int resolve_kernel(const das_plan_s *p)
+{
+    const bool cplx = p->dtype == DAS_C64;
+    if (p->kernel != DAS_KERNEL_AUTO) return p->kernel;
+    if (das::brick_supported(p->B, cplx, p->K)) return DAS_KERNEL_BRICK;
+    if (p->K >= 2 && das::bi_supported(p->B, cplx, p->bi_group)) return DAS_KERNEL_BI;
+    return DAS_KERNEL_BL;
+}
+
+das_status check_supported(const das_plan_s *p, int kernel)
+{
+    const bool cplx = p->dtype == DAS_C64;
+    switch (kernel) {
+    case DAS_KERNEL_BL: return DAS_OK;
+    case DAS_KERNEL_BI:
+        if (p->K < 2 || !das::bi_supported(p->B, cplx, p->bi_group))
+            return fail(DAS_ERR_UNSUPPORTED,
+                        "BI kernel needs K >= 2 and B a multiple of the group's 16-byte chunks "
+                        "(B=%d, group=%d)", p->B, p->bi_group);
+        return DAS_OK;
+    case DAS_KERNEL_BRICK:
+        if (!das::brick_supported(p->B, cplx, p->K))
+            return fail(DAS_ERR_UNSUPPORTED,
+                        "brick kernel needs K >= 2 and B*element size in {32, 64, 128, 256, 512} "
+                        "bytes (B=%d)", p->B);
+        return DAS_OK;
+    default: return fail(DAS_ERR_INVALID_ARG, "unknown kernel %d", kernel);
+    }
+}
+
+void release(das_plan_s *p)
+{
+    cudaFree(p->d_rx);
+    cudaFree(p->d_perm);
+    cudaFree(p->d_rf);
+    cudaFree(p->d_out);
+    cudaFree(p->d_tau);
+    cudaFree(p->d_w);
+    for (auto &e : p->ev)
+        if (e) cudaEventDestroy(e);
+}
+
+// Restores the caller's current device on scope exit.
+struct DeviceGuard {
+    int prev = -1;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) cudaSetDevice(dev);
+        else prev = -1;
+    }
+    ~DeviceGuard()
+    {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+}  // namespace
+
+extern "C" {
+
+const char *das_last_error_string(void) { return g_err; }
+
+const char *das_version(void) { return "1.0.0"; }
+
+das_status das_plan_create(das_plan *plan, const das_grid *grid, const float *rx_xyz, float c,
+                           float fs, float t0, float fnum, das_dtype dtype, int B, int Q, int M,
+                           int K)
+{
+    g_err[0] = '\0';
+    if (!plan) return fail(DAS_ERR_INVALID_ARG, "plan is NULL");
+    *plan = nullptr;
+    if (!grid) return fail(DAS_ERR_INVALID_ARG, "grid is NULL");
+    if (!rx_xyz) return fail(DAS_ERR_INVALID_ARG, "rx_xyz is NULL");
+    if (grid->nx < 1 || grid->ny < 1 || grid->nz < 1)
+        return fail(DAS_ERR_INVALID_ARG, "grid dimensions must be >= 1");
+    const float gf[6] = {grid->x0, grid->y0, grid->z0, grid->dx, grid->dy, grid->dz};
+    for (float v : gf)
+        if (!std::isfinite(v)) return fail(DAS_ERR_INVALID_ARG, "grid origin/spacing not finite");
+    if (!(c > 0.f) || !std::isfinite(c)) return fail(DAS_ERR_INVALID_ARG, "c must be > 0");
+    if (!(fs > 0.f) || !std::isfinite(fs)) return fail(DAS_ERR_INVALID_ARG, "fs must be > 0");
+    if (!std::isfinite(t0) || !std::isfinite(fnum))
+        return fail(DAS_ERR_INVALID_ARG, "t0 and fnum must be finite");
+    if (dtype != DAS_F32 && dtype != DAS_C64) return fail(DAS_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (B < 1 || Q < 1 || M < 1 || K < 1) return fail(DAS_ERR_INVALID_ARG, "B, Q, M, K must be >= 1");
+    const long long N = (long long)grid->nx * grid->ny * grid->nz;
+    if ((long long)Q * M * K >= (1LL << 31)) return fail(DAS_ERR_INVALID_ARG, "Q*M*K must be < 2^31");
+    if (N * B >= (1LL << 31)) return fail(DAS_ERR_INVALID_ARG, "B*N must be < 2^31");
+    if ((long long)Q * N >= (1LL << 40)) return fail(DAS_ERR_INVALID_ARG, "Q*N too large");
+    if (K >= (1 << 22)) return fail(DAS_ERR_INVALID_ARG, "K must be < 2^22");
+    for (int i = 0; i < 3 * M; ++i)
+        if (!std::isfinite(rx_xyz[i])) return fail(DAS_ERR_INVALID_ARG, "receiver position not finite");
+
+    das_plan_s *p = new (std::nothrow) das_plan_s;
+    if (!p) return fail(DAS_ERR_OUT_OF_MEMORY, "host allocation of the plan failed");
+    p->grid = *grid;
+    p->c = c; p->fs = fs; p->t0 = t0; p->fnum = fnum;
+    p->dtype = dtype;
+    p->B = B; p->Q = Q; p->M = M; p->K = K;
+    p->N = N;
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e != cudaSuccess) { delete p; return cuda_fail(e, "cudaGetDevice"); }
+    e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+    if (e != cudaSuccess) { delete p; return cuda_fail(e, "cudaDeviceGetAttribute"); }
+
+    // positions in sample units (metres * fs / c), scaled in double
+    const double s = (double)fs / (double)c;
+    std::vector<RxPos> hrx(M);
+    for (int m = 0; m < M; ++m)
+        hrx[m] = make_float4((float)(rx_xyz[3 * m] * s), (float)(rx_xyz[3 * m + 1] * s),
+                             (float)(rx_xyz[3 * m + 2] * s), 0.f);
+    DasGeom &g = p->geom;
+    g.nx = grid->nx; g.ny = grid->ny; g.nz = grid->nz; g.N = (int)N;
+    g.x0 = (float)(grid->x0 * s); g.y0 = (float)(grid->y0 * s); g.z0 = (float)(grid->z0 * s);
+    g.dx = (float)(grid->dx * s); g.dy = (float)(grid->dy * s); g.dz = (float)(grid->dz * s);
+    g.fs = fs;
+    g.t0fs = (float)((double)t0 * fs);
+    g.aperture = fnum > 0.f;
+    g.ap2 = g.aperture ? (float)(4.0 * (double)fnum * fnum) : 0.f;
+    g.fd_over_fs = 0.f;
+    g.rotate = 0;
+    g.B = B; g.Q = Q; g.M = M; g.K = K;
+
+    e = cudaMalloc(&p->d_rx, sizeof(RxPos) * M);
+    if (e == cudaSuccess) e = cudaMemcpy(p->d_rx, hrx.data(), sizeof(RxPos) * M, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+        release(p);
+        delete p;
+        return cuda_fail(e, "receiver upload");
+    }
+    *plan = p;
+    return DAS_OK;
+}
+
+das_status das_plan_set_option(das_plan p, int option, double value)
+{
+    if (!p) return fail(DAS_ERR_INVALID_ARG, "plan is NULL");
+    switch (option) {
+    case DAS_OPT_KERNEL: {
+        const int k = (int)value;
+        if ((double)k != value || k < DAS_KERNEL_AUTO || k > DAS_KERNEL_BRICK)
+            return fail(DAS_ERR_INVALID_ARG, "invalid kernel %g", value);
+        p->kernel = k;
+        return DAS_OK;
+    }
+    case DAS_OPT_DEMOD_HZ:
+        if (!std::isfinite(value)) return fail(DAS_ERR_INVALID_ARG, "f_demod must be finite");
+        if (p->dtype != DAS_C64 && value != 0.0)
+            return fail(DAS_ERR_UNSUPPORTED, "demodulation needs a DAS_C64 plan");
+        p->f_demod = value;
+        p->geom.fd_over_fs = (float)(value / (double)p->fs);
+        p->geom.rotate = value != 0.0;
+        return DAS_OK;
+    case DAS_OPT_TIMING:
+        if (value != 0.0 && value != 1.0) return fail(DAS_ERR_INVALID_ARG, "timing must be 0 or 1");
+        if (value == 1.0 && !p->ev[0]) {
+            DeviceGuard dg(p->device);
+            for (auto &ev : p->ev) {
+                cudaError_t e = cudaEventCreate(&ev);
+                if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+            }
+        }
+        p->timing = (int)value;
+        p->timed_once = false;
+        return DAS_OK;
+    case DAS_OPT_BI_GROUP: {
+        const int gsz = (int)value;
+        if ((double)gsz != value || !(gsz == 0 || gsz == 2 || gsz == 4 || gsz == 8 || gsz == 16 || gsz == 32))
+            return fail(DAS_ERR_INVALID_ARG, "BI group must be 0, 2, 4, 8, 16 or 32");
+        p->bi_group = gsz;
+        return DAS_OK;
+    }
+    default: return fail(DAS_ERR_INVALID_ARG, "unknown option %d", option);
+    }
+}
+
+das_status das_plan_get_option(das_plan p, int option, double *value)
+{
+    if (!p || !value) return fail(DAS_ERR_INVALID_ARG, "NULL argument");
+    switch (option) {
+    case DAS_OPT_KERNEL: *value = p->kernel; return DAS_OK;
+    case DAS_OPT_DEMOD_HZ: *value = p->f_demod; return DAS_OK;
+    case DAS_OPT_TIMING: *value = p->timing; return DAS_OK;
+    case DAS_OPT_BI_GROUP: *value = p->bi_group; return DAS_OK;
+    default: return fail(DAS_ERR_INVALID_ARG, "unknown option %d", option);
+    }
+}
+
+das_status das_plan_kernel(das_plan p, int *kernel)
+{
+    if (!p || !kernel) return fail(DAS_ERR_INVALID_ARG, "NULL argument");
+    *kernel = resolve_kernel(p);
+    return DAS_OK;
+}
+
+das_status das_beamform(das_plan p, const void *rf, const float *tau_tx, const float *w_tx,
+                        void *out, cudaStream_t stream)
+{
+    if (!p) return fail(DAS_ERR_INVALID_ARG, "plan is NULL");
+    if (!rf || !tau_tx || !w_tx || !out) return fail(DAS_ERR_INVALID_ARG, "NULL buffer");
+    if (!aligned16(rf) || !aligned16(out))
+        return fail(DAS_ERR_INVALID_ARG, "rf and out must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(tau_tx) & 3u) || (reinterpret_cast<uintptr_t>(w_tx) & 3u))
+        return fail(DAS_ERR_INVALID_ARG, "tau_tx and w_tx must be 4-byte aligned");
+    const int kernel = resolve_kernel(p);
+    das_status st = check_supported(p, kernel);
+    if (st != DAS_OK) return st;
+    DeviceGuard dg(p->device);
+    const bool cplx = p->dtype == DAS_C64;
+
+    const void *src = rf;
+    const bool permute = kernel != DAS_KERNEL_BL;
+    if (permute && !p->d_perm) {
+        cudaError_t e = cudaMalloc(&p->d_perm, p->rf_bytes());
+        if (e != cudaSuccess) {
+            p->d_perm = nullptr;
+            cudaGetLastError();
+            return cuda_fail(e, "permute scratch allocation");
+        }
+        p->perm_bytes = p->rf_bytes();
+    }
+    cudaError_t e = cudaSuccess;
+    if (p->timing) e = cudaEventRecord(p->ev[0], stream);
+    if (e == cudaSuccess && permute) {
+        e = das::launch_permute(rf, p->d_perm, (int)p->elem_bytes(), p->B, p->Q, p->M, p->K,
+                                kernel == DAS_KERNEL_BI ? 0 : 1, p->num_sms, stream);
+        src = p->d_perm;
+    }
+    if (e == cudaSuccess && p->timing) e = cudaEventRecord(p->ev[1], stream);
+    if (e != cudaSuccess) return cuda_fail(e, "permute launch");
+    switch (kernel) {
+    case DAS_KERNEL_BL: e = das::launch_bl(p->geom, p->d_rx, src, tau_tx, w_tx, out, cplx, stream); break;
+    case DAS_KERNEL_BI:
+        e = das::launch_bi(p->geom, p->d_rx, src, tau_tx, w_tx, out, cplx, p->bi_group, stream);
+        break;
+    default: e = das::launch_brick(p->geom, p->d_rx, src, tau_tx, w_tx, out, cplx, stream); break;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "DAS kernel launch");
+    if (p->timing) {
+        e = cudaEventRecord(p->ev[2], stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+        p->timed_once = true;
+        p->last_had_permute = permute;
+    }
+    return DAS_OK;
+}
+
+das_status das_beamform_host(das_plan p, const void *rf_host, const float *tau_tx_host,
+                             const float *w_tx_host, void *out_host, cudaStream_t stream)
+{
+    if (!p) return fail(DAS_ERR_INVALID_ARG, "plan is NULL");
+    if (!rf_host || !tau_tx_host || !w_tx_host || !out_host) return fail(DAS_ERR_INVALID_ARG, "NULL buffer");
+    DeviceGuard dg(p->device);
+    cudaError_t e = cudaSuccess;
+    if (!p->d_rf) e = cudaMalloc(&p->d_rf, p->rf_bytes());
+    if (e == cudaSuccess && !p->d_out) e = cudaMalloc(&p->d_out, p->out_bytes());
+    if (e == cudaSuccess && !p->d_tau) e = cudaMalloc(&p->d_tau, p->txw_bytes());
+    if (e == cudaSuccess && !p->d_w) e = cudaMalloc(&p->d_w, p->txw_bytes());
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return cuda_fail(e, "host-path device buffers");
+    }
+    e = cudaMemcpyAsync(p->d_rf, rf_host, p->rf_bytes(), cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(p->d_tau, tau_tx_host, p->txw_bytes(), cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(p->d_w, w_tx_host, p->txw_bytes(), cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+    das_status st = das_beamform(p, p->d_rf, p->d_tau, p->d_w, p->d_out, stream);
+    if (st != DAS_OK) return st;
+    e = cudaMemcpyAsync(out_host, p->d_out, p->out_bytes(), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
+    return DAS_OK;
+}
+
+das_status das_plan_last_times(das_plan p, float *permute_ms, float *das_ms)
+{
+    if (!p || !permute_ms || !das_ms) return fail(DAS_ERR_INVALID_ARG, "NULL argument");
+    if (!p->timing || !p->timed_once) return fail(DAS_ERR_INVALID_ARG, "no timed call recorded");
+    DeviceGuard dg(p->device);
+    cudaError_t e = cudaEventSynchronize(p->ev[2]);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(permute_ms, p->ev[0], p->ev[1]);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(das_ms, p->ev[1], p->ev[2]);
+    if (e != cudaSuccess) return cuda_fail(e, "event timing");
+    if (!p->last_had_permute) *permute_ms = 0.f;
+    return DAS_OK;
+}
+
+das_status das_plan_device_bytes(das_plan p, size_t *bytes)
+{
+    if (!p || !bytes) return fail(DAS_ERR_INVALID_ARG, "NULL argument");
+    size_t b = sizeof(RxPos) * p->M + p->perm_bytes;
+    if (p->d_rf) b += p->rf_bytes();
+    if (p->d_out) b += p->out_bytes();
+    if (p->d_tau) b += p->txw_bytes();
+    if (p->d_w) b += p->txw_bytes();
+    *bytes = b;
+    return DAS_OK;
+}
+
+das_status das_plan_destroy(das_plan p)
+{
+    if (!p) return DAS_OK;
+    {
+        DeviceGuard dg(p->device);
+        cudaDeviceSynchronize();
+        release(p);
+    }
+    delete p;
+    return DAS_OK;
+}
+
+das_status das_permute(const void *in, void *out, das_dtype dtype, int B, int Q, int M, int K,
+                       int layout, cudaStream_t stream)
+{
+    if (!in || !out) return fail(DAS_ERR_INVALID_ARG, "NULL buffer");
+    if (dtype != DAS_F32 && dtype != DAS_C64) return fail(DAS_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (B < 1 || Q < 1 || M < 1 || K < 1) return fail(DAS_ERR_INVALID_ARG, "B, Q, M, K must be >= 1");
+    if ((long long)Q * M >= (1LL << 31)) return fail(DAS_ERR_INVALID_ARG, "Q*M must be < 2^31");
+    if (layout != 0 && layout != 1) return fail(DAS_ERR_INVALID_ARG, "layout must be 0 or 1");
+    const size_t eb = dtype == DAS_C64 ? 8 : 4;
+    const size_t bytes = (size_t)B * Q * M * K * eb;
+    const char *a = static_cast<const char *>(in);
+    const char *b = static_cast<const char *>(out);
+    if (a < b + bytes && b < a + bytes) return fail(DAS_ERR_INVALID_ARG, "in and out overlap");
+    int dev = 0, sms = 1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = das::launch_permute(in, out, (int)eb, B, Q, M, K, layout, sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "permute");
+    return DAS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,43 @@
+// Internal definitions shared by the libdas CUDA sources (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "das.h"
+
+// Geometry and sizes handed to every DAS kernel by value.  Positions are kept
+// in sample units (metres * fs / c), so |x_n - r_m| is directly the receive
+// delay in samples and the fractional index is f = tau_tx * fs - t0 * fs + d.
+struct DasGeom {
+    int nx, ny, nz;
+    int N;                // nx * ny * nz
+    float x0, y0, z0;     // first voxel, sample units
+    float dx, dy, dz;     // grid spacing, sample units
+    float fs;             // Hz, converts tau_tx (s) to samples
+    float t0fs;           // t0 * fs
+    float ap2;            // (2 F#)^2
+    int aperture;         // 0: F# <= 0, every receiver counts
+    float fd_over_fs;     // demodulation cycles per sample (IQ)
+    int rotate;           // 1: apply the IQ phase
+    int B, Q, M, K;
+};
+
+// Receiver record of the plan: position in sample units.
+using RxPos = float4;
+
+namespace das {
+
+// Launchers (each returns the cudaError_t of its launch).
+cudaError_t launch_permute(const void *in, void *out, int elem_bytes, int B, int Q, int M, int K,
+                           int layout, int num_sms, cudaStream_t stream);
+cudaError_t launch_bl(const DasGeom &g, const RxPos *rx, const void *rf, const float *tau,
+                      const float *w, void *out, bool cplx, cudaStream_t stream);
+bool bi_supported(int B, bool cplx, int group);
+cudaError_t launch_bi(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
+                      const float *w, void *out, bool cplx, int group, cudaStream_t stream);
+bool brick_supported(int B, bool cplx, int K);
+cudaError_t launch_brick(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
+                         const float *w, void *out, bool cplx, cudaStream_t stream);
+
+}  // namespace das

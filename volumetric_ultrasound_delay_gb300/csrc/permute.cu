@@ -1,0 +1,139 @@
+// RF layout permute: B x Q x M x K (k contiguous) -> a b-contiguous layout,
+// as the batch-inner design needs (ffdas paper, Methods, batch-inner
+// paragraph; ffdas docs, ALG2: the permute runs as part of the launch).
+//
+// For every (q, m) the (b, k) plane is transposed through shared memory in
+// 32 x 32 element tiles, two tiles per block iteration so each thread keeps two
+// 16-byte loads in flight.  Global loads read 16-byte vectors along k, global
+// stores write 16-byte vectors along b; the shared tile has one element of
+// padding per row, so the scalar shared-memory traffic is conflict-free for
+// 4-byte elements.  The copy moves opaque element values and is bit-exact.
+//
+//   layout 0: out[((k*Q + q)*M + m)*B + b]   (K x Q x M x B)
+//   layout 1: out[((q*M + m)*K + k)*B + b]   (Q x M x K x B)
+#include <cstdint>
+#include <cstring>
+
+#include "das_internal.cuh"
+
+namespace das {
+namespace {
+
+constexpr int TILE = 32;
+constexpr int SUB = 2;           // tiles along k per block iteration
+constexpr int THREADS = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(THREADS)
+permute_kernel(const T *__restrict__ in, T *__restrict__ out, int B, int QM, int K,
+               long long osk, long long osqm, long long n_blocks, int blocks_b, int blocks_k,
+               int vec_in, int vec_out)
+{
+    constexpr int V = 16 / sizeof(T);            // elements per 16-byte vector
+    constexpr int VPR = TILE / V;                // vectors per 32-element row
+    __shared__ T tile[SUB][TILE][TILE + 1];
+    const int tid = threadIdx.x;
+
+    for (long long t = blockIdx.x; t < n_blocks; t += gridDim.x) {
+        const int tk = (int)(t % blocks_k);
+        const long long r = t / blocks_k;
+        const int tb = (int)(r % blocks_b);
+        const int qm = (int)(r / blocks_b);
+        const int b0 = tb * TILE;
+        const int k0 = tk * TILE * SUB;
+
+        // ---- load SUB tiles of 32 (b) x 32 (k)
+        if (vec_in) {
+#pragma unroll
+            for (int s = 0; s < SUB; ++s) {
+                for (int i = tid; i < TILE * VPR; i += THREADS) {
+                    const int row = i / VPR, v = i % VPR;
+                    const int b = b0 + row, k = k0 + s * TILE + v * V;
+                    if (b < B && k < K) {   // K % V == 0, so the whole vector is inside
+                        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(
+                            in + ((long long)b * QM + qm) * K + k));
+                        T vals[V];
+                        memcpy(vals, &u, sizeof(u));
+#pragma unroll
+                        for (int j = 0; j < V; ++j) tile[s][row][v * V + j] = vals[j];
+                    }
+                }
+            }
+        } else {
+            for (int s = 0; s < SUB; ++s)
+                for (int i = tid; i < TILE * TILE; i += THREADS) {
+                    const int row = i / TILE, kk = i % TILE;
+                    const int b = b0 + row, k = k0 + s * TILE + kk;
+                    if (b < B && k < K) tile[s][row][kk] = in[((long long)b * QM + qm) * K + k];
+                }
+        }
+        __syncthreads();
+
+        // ---- store: rows of k, b contiguous
+        if (vec_out) {
+#pragma unroll
+            for (int s = 0; s < SUB; ++s) {
+                for (int i = tid; i < TILE * VPR; i += THREADS) {
+                    const int krow = i / VPR, v = i % VPR;
+                    const int k = k0 + s * TILE + krow, b = b0 + v * V;
+                    if (k < K && b < B) {   // B % V == 0
+                        T vals[V];
+#pragma unroll
+                        for (int j = 0; j < V; ++j) vals[j] = tile[s][v * V + j][krow];
+                        uint4 u;
+                        memcpy(&u, vals, sizeof(u));
+                        *reinterpret_cast<uint4 *>(out + (long long)k * osk + (long long)qm * osqm + b) = u;
+                    }
+                }
+            }
+        } else {
+            for (int s = 0; s < SUB; ++s)
+                for (int i = tid; i < TILE * TILE; i += THREADS) {
+                    const int krow = i / TILE, bb = i % TILE;
+                    const int k = k0 + s * TILE + krow, b = b0 + bb;
+                    if (k < K && b < B)
+                        out[(long long)k * osk + (long long)qm * osqm + b] = tile[s][bb][krow];
+                }
+        }
+        __syncthreads();
+    }
+}
+
+template <typename T>
+cudaError_t launch_typed(const void *in, void *out, int B, int Q, int M, int K, int layout,
+                         int num_sms, cudaStream_t stream)
+{
+    constexpr int V = 16 / sizeof(T);
+    const int QM = Q * M;
+    const long long osk = layout == 0 ? (long long)QM * B : (long long)B;
+    const long long osqm = layout == 0 ? (long long)B : (long long)K * B;
+    const int blocks_b = (B + TILE - 1) / TILE;
+    const int blocks_k = (K + TILE * SUB - 1) / (TILE * SUB);
+    const long long n_blocks = (long long)QM * blocks_b * blocks_k;
+    if (n_blocks == 0) return cudaSuccess;
+    const bool in_al = (reinterpret_cast<uintptr_t>(in) % 16) == 0;
+    const bool out_al = (reinterpret_cast<uintptr_t>(out) % 16) == 0;
+    const int vec_in = in_al && (K % V == 0);
+    const int vec_out = out_al && (B % V == 0) && (osk % V == 0) && (osqm % V == 0);
+    const long long cap = (long long)num_sms * 8;
+    const int grid = (int)(n_blocks < cap ? n_blocks : cap);
+    permute_kernel<T><<<grid, THREADS, 0, stream>>>(
+        static_cast<const T *>(in), static_cast<T *>(out), B, QM, K, osk, osqm, n_blocks,
+        blocks_b, blocks_k, vec_in, vec_out);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const void *in, void *out, int elem_bytes, int B, int Q, int M, int K,
+                           int layout, int num_sms, cudaStream_t stream)
+{
+    switch (elem_bytes) {
+    case 2: return launch_typed<unsigned short>(in, out, B, Q, M, K, layout, num_sms, stream);
+    case 4: return launch_typed<float>(in, out, B, Q, M, K, layout, num_sms, stream);
+    case 8: return launch_typed<float2>(in, out, B, Q, M, K, layout, num_sms, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace das

@@ -1,0 +1,219 @@
+"""Thin Python binding of libdas (ctypes; argument marshalling only).
+
+Every step of the computation runs in the CUDA library: this module only
+loads ``_lib/libdas.so``, checks tensor arguments and forwards raw pointers and
+the current torch stream.  There is no fallback: if the library is missing the
+import of :func:`lib` raises, so a GPU path can never silently run elsewhere.
+
+Names follow the C ABI in ``include/das.h``: :class:`Plan` wraps
+``das_plan_create`` / ``das_beamform`` / ``das_plan_destroy``, :func:`permute`
+wraps ``das_permute``.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import numpy as np
+
+LIBRARY = Path(__file__).resolve().parent / "_lib" / "libdas.so"
+
+DAS_OK, DAS_ERR_INVALID_ARG, DAS_ERR_UNSUPPORTED, DAS_ERR_OUT_OF_MEMORY, DAS_ERR_CUDA, \
+    DAS_ERR_TIMEOUT = range(6)
+DAS_F32, DAS_C64 = 0, 1
+KERNELS = {"auto": 0, "bl": 1, "bi": 2, "brick": 3}
+KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
+OPT_KERNEL, OPT_DEMOD_HZ, OPT_TIMING, OPT_BI_GROUP = 0, 1, 2, 3
+
+# every function the header declares, with its ctypes signature
+_VP = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_SIGS = {
+    "das_plan_create": (_I, [ctypes.POINTER(_VP), _VP, _VP, _F, _F, _F, _F, _I, _I, _I, _I, _I]),
+    "das_plan_set_option": (_I, [_VP, _I, ctypes.c_double]),
+    "das_plan_get_option": (_I, [_VP, _I, ctypes.POINTER(ctypes.c_double)]),
+    "das_plan_kernel": (_I, [_VP, ctypes.POINTER(_I)]),
+    "das_beamform": (_I, [_VP, _VP, _VP, _VP, _VP, _VP]),
+    "das_beamform_host": (_I, [_VP, _VP, _VP, _VP, _VP, _VP]),
+    "das_plan_last_times": (_I, [_VP, ctypes.POINTER(_F), ctypes.POINTER(_F)]),
+    "das_plan_device_bytes": (_I, [_VP, ctypes.POINTER(ctypes.c_size_t)]),
+    "das_plan_destroy": (_I, [_VP]),
+    "das_permute": (_I, [_VP, _VP, _I, _I, _I, _I, _I, _I, _VP]),
+    "das_last_error_string": (ctypes.c_char_p, []),
+    "das_version": (ctypes.c_char_p, []),
+}
+
+
+class DasError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"libdas error {status}: {message}")
+        self.status = status
+
+
+class _Grid(ctypes.Structure):
+    _fields_ = [("nx", _I), ("ny", _I), ("nz", _I),
+                ("x0", _F), ("y0", _F), ("z0", _F), ("dx", _F), ("dy", _F), ("dz", _F)]
+
+
+_LIB = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libdas (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not LIBRARY.exists():
+            raise ImportError(f"libdas.so not built ({LIBRARY}); run __graft_entry__.build()")
+        h = ctypes.CDLL(str(LIBRARY))
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(h, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = h
+    return _LIB
+
+
+def _check(status: int):
+    if status != DAS_OK:
+        raise DasError(status, lib().das_last_error_string().decode())
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev_ptr(t, name, dtype=None, numel=None):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must have {numel} elements, got {t.numel()}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+class Plan:
+    """A DAS plan: fixed grid, receivers, physics constants, dtype and sizes."""
+
+    def __init__(self, grid, rx_xyz, c, fs, t0=0.0, fnum=0.0, dtype="f32", B=1, Q=1, M=None,
+                 K=1, kernel="auto", f_demod=0.0):
+        rx = np.ascontiguousarray(rx_xyz, dtype=np.float32).reshape(-1, 3)
+        M = rx.shape[0] if M is None else M
+        if M != rx.shape[0]:
+            raise ValueError("M does not match rx_xyz")
+        self.grid = tuple(grid)
+        self.dtype = dtype
+        self.B, self.Q, self.M, self.K = int(B), int(Q), int(M), int(K)
+        self.N = self.grid[0] * self.grid[1] * self.grid[2]
+        g = _Grid(*[int(v) for v in self.grid[:3]], *[float(v) for v in self.grid[3:]])
+        h = ctypes.c_void_p()
+        dt = {"f32": DAS_F32, "c64": DAS_C64}[dtype]
+        self._rx = rx
+        _check(lib().das_plan_create(ctypes.byref(h), ctypes.byref(g),
+                                     rx.ctypes.data_as(ctypes.c_void_p), c, fs, t0, fnum, dt,
+                                     self.B, self.Q, self.M, self.K))
+        self._h = h
+        if kernel != "auto":
+            self.set_option(OPT_KERNEL, KERNELS[kernel])
+        if f_demod:
+            self.set_option(OPT_DEMOD_HZ, f_demod)
+
+    # -- options
+    def set_option(self, opt: int, value: float):
+        _check(lib().das_plan_set_option(self._h, opt, float(value)))
+
+    def get_option(self, opt: int) -> float:
+        v = ctypes.c_double()
+        _check(lib().das_plan_get_option(self._h, opt, ctypes.byref(v)))
+        return v.value
+
+    @property
+    def kernel(self) -> str:
+        k = ctypes.c_int()
+        _check(lib().das_plan_kernel(self._h, ctypes.byref(k)))
+        return KERNEL_NAMES[k.value]
+
+    @kernel.setter
+    def kernel(self, name: str):
+        self.set_option(OPT_KERNEL, KERNELS[name])
+
+    # -- compute
+    def _torch_dtypes(self):
+        import torch
+        return torch.float32, (torch.complex64 if self.dtype == "c64" else torch.float32)
+
+    def beamform(self, rf, tau_tx, w_tx, out=None, stream=None):
+        """y (B x N) from device tensors rf (B x Q x M x K), tau_tx / w_tx (Q x N)."""
+        import torch
+        f32, el = self._torch_dtypes()
+        if out is None:
+            out = torch.empty((self.B, self.N), dtype=el, device=rf.device)
+        _check(lib().das_beamform(
+            self._h, _dev_ptr(rf, "rf", el, self.B * self.Q * self.M * self.K),
+            _dev_ptr(tau_tx, "tau_tx", f32, self.Q * self.N), _dev_ptr(w_tx, "w_tx", f32, self.Q * self.N),
+            _dev_ptr(out, "out", el, self.B * self.N), _stream_handle(stream)))
+        return out
+
+    def beamform_host(self, rf, tau_tx, w_tx, out, stream=None):
+        """Same computation from host arrays/tensors (copies inside, synchronous)."""
+        def hp(a, name, n):
+            import torch
+            if isinstance(a, torch.Tensor):
+                if a.is_cuda or not a.is_contiguous() or a.numel() != n:
+                    raise ValueError(f"{name} must be a contiguous host tensor of {n} elements")
+                return ctypes.c_void_p(a.data_ptr())
+            if not (isinstance(a, np.ndarray) and a.flags.c_contiguous and a.size == n):
+                raise ValueError(f"{name} must be a contiguous host array of {n} elements")
+            return a.ctypes.data_as(ctypes.c_void_p)
+        _check(lib().das_beamform_host(
+            self._h, hp(rf, "rf", self.B * self.Q * self.M * self.K),
+            hp(tau_tx, "tau_tx", self.Q * self.N), hp(w_tx, "w_tx", self.Q * self.N),
+            hp(out, "out", self.B * self.N), _stream_handle(stream)))
+        return out
+
+    def last_times(self):
+        """(permute_ms, das_ms) of the last beamform when timing is on."""
+        a, b = ctypes.c_float(), ctypes.c_float()
+        _check(lib().das_plan_last_times(self._h, ctypes.byref(a), ctypes.byref(b)))
+        return a.value, b.value
+
+    def device_bytes(self) -> int:
+        v = ctypes.c_size_t()
+        _check(lib().das_plan_device_bytes(self._h, ctypes.byref(v)))
+        return v.value
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _check(lib().das_plan_destroy(self._h))
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def permute(rf, out, layout: int = 0, stream=None):
+    """Bit-exact B x Q x M x K -> K x Q x M x B (layout 0) or Q x M x K x B (layout 1)."""
+    import torch
+    if rf.dtype not in (torch.float32, torch.complex64) or rf.dim() != 4:
+        raise TypeError("rf must be a 4-D float32 or complex64 CUDA tensor")
+    B, Q, M, K = rf.shape
+    dt = DAS_C64 if rf.dtype == torch.complex64 else DAS_F32
+    _check(lib().das_permute(_dev_ptr(rf, "rf"), _dev_ptr(out, "out", rf.dtype, rf.numel()), dt,
+                             B, Q, M, K, layout, _stream_handle(stream)))
+    return out
