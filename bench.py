@@ -57,7 +57,20 @@ def parse_args():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--n-el", type=int, default=None, help="override: array elements per side")
+    ap.add_argument("--grid", type=int, nargs=3, default=None, metavar=("NX", "NY", "NZ"),
+                    help="override: voxel grid (for small profiling cases)")
     return ap.parse_args()
+
+
+def make_workload(args):
+    from volumetric_ultrasound_delay_gb300 import synth
+    kw = {}
+    if args.n_el:
+        kw["n_el"] = args.n_el
+    if args.grid:
+        kw["nx"], kw["ny"], kw["nz"] = args.grid
+    return synth.make_problem(args.workload, **kw)
 
 
 def describe(wl) -> str:
@@ -221,7 +234,7 @@ def run_reference(args, world, rank):
     from volumetric_ultrasound_delay_gb300 import synth
     import oracle
     oracle.build()
-    prob = synth.make_problem(args.workload)
+    prob = make_workload(args)
     cores = os.cpu_count() or 1
     per_step = max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
     # size one step's voxel sample from a probe run
@@ -262,7 +275,7 @@ def run_ours(args, world, rank, local):
     libbuild.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    prob = synth.make_problem(args.workload)
+    prob = make_workload(args)
     dtype = "c64" if prob.wl.iq else "f32"
     A = prob.B * prob.N * prob.Q * prob.M
     rf = torch.from_numpy(prob.rf).to(dev)

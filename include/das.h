@@ -72,7 +72,7 @@ typedef enum {
     DAS_KERNEL_BRICK = 3   /* this library's sm_103a design: voxel bricks per CTA,
                               per-(voxel, transmit, receiver) geometry staged in
                               shared memory, receivers outside every aperture of
-                              the brick skipped, Q x M x K x B copy */
+                              the brick skipped, zero-padded Q x M x (K+3) x B copy */
 } das_kernel;
 
 /* Plan options. */
@@ -104,9 +104,9 @@ typedef struct {
  *   fnum     receive F-number; <= 0 disables the aperture.
  *   dtype    DAS_F32 or DAS_C64.
  *   B,Q,M,K  frames, transmits, receivers, samples per record (all >= 1);
- *            Q*M*K and B*N must stay below 2^31, K below 2^22.
+ *            Q*M*(K+3) and B*N must stay below 2^31, K below 2^22.
  * Allocates the device copies of the geometry; the permute scratch of the BI
- * and brick kernels (B*Q*M*K elements) is allocated on first use.
+ * and brick kernels (B*Q*M*(K+3) elements) is allocated on first use.
  * Errors: DAS_ERR_INVALID_ARG, DAS_ERR_OUT_OF_MEMORY, DAS_ERR_CUDA; *plan is
  * set to NULL on failure.  The plan belongs to the device current at creation.
  */
@@ -167,9 +167,14 @@ das_status das_plan_destroy(das_plan plan);
 /*
  * RF layout permute (ffdas paper, Methods, batch-inner paragraph: B x Q x M x K
  * with k contiguous -> a layout with b contiguous).  A bit-exact copy.
- *   layout 0: K x Q x M x B (the pages' batch-inner layout)
- *   layout 1: Q x M x K x B (rows of one (q, m) adjacent; used by the brick kernel)
- *   in, out  device buffers of B*Q*M*K elements of dtype, not overlapping.
+ *   layout 0: K x Q x M x B (the pages' batch-inner layout, used by BI)
+ *   layout 1: Q x M x K x B (rows of one (q, m) adjacent)
+ *   layout 2: Q x M x (K+3) x B, sample k of slab (q, m) at row k + 1; rows 0,
+ *             K + 1 and K + 2 of every slab are not written (the brick kernel
+ *             keeps them zero, so reads just outside the record return 0)
+ *   in       device buffer of B*Q*M*K elements of dtype;
+ *   out      device buffer of B*Q*M*K (layouts 0, 1) or B*Q*M*(K+3) (layout 2)
+ *            elements; in and out must not overlap.
  * Errors: DAS_ERR_INVALID_ARG, DAS_ERR_CUDA.  Asynchronous.
  */
 das_status das_permute(const void *in, void *out, das_dtype dtype, int B, int Q, int M,

@@ -48,7 +48,7 @@ def small_problems():
 @pytest.mark.parametrize("shape", [(32, 9, 16, 2048), (16, 3, 7, 100), (3, 2, 5, 37),
                                    (1, 1, 1, 1), (5, 1, 3, 64), (40, 2, 3, 33)])
 @pytest.mark.parametrize("dtype", ["f32", "c64"])
-@pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("layout", [0, 1, 2])
 def test_permute_bit_exact(oracle, shape, dtype, layout):
     from volumetric_ultrasound_delay_gb300 import das
     rng = np.random.default_rng(zlib.crc32(repr((shape, dtype, layout)).encode()))
@@ -57,6 +57,18 @@ def test_permute_bit_exact(oracle, shape, dtype, layout):
     else:
         x = rng.standard_normal(shape).astype(np.float32)
     src = torch.from_numpy(x).cuda()
+    B, Q, M, K = shape
+    if layout == 2:
+        # padded slabs: data rows 1..K of each (q, m) slab, pad rows left as they were
+        dst = torch.full((Q * M * (K + 3) * B,), 7.5, dtype=src.dtype, device="cuda")
+        das.permute(src, dst, layout)
+        torch.cuda.synchronize()
+        got = dst.cpu().numpy().reshape(Q, M, K + 3, B)
+        want = oracle.permute(x, "qmkb")
+        assert got[:, :, 1:K + 1].tobytes() == want.tobytes()
+        pads = np.concatenate([got[:, :, :1], got[:, :, K + 1:]], axis=2)
+        assert np.all(pads == np.asarray(7.5, dtype=x.dtype))
+        return
     dst = torch.empty_like(src).reshape(-1)
     das.permute(src, dst, layout)
     torch.cuda.synchronize()
@@ -137,7 +149,7 @@ def test_nan_delay_contributes_nothing(oracle):
     ref, slack = oracle_beamform(oracle, prob)
     for kernel in KERNELS:
         y, _ = gpu_beamform(prob, kernel)
-        assert np.all(np.isfinite(y))
+        assert np.all(np.isfinite(y)), kernel
         assert error_ratio(y, ref, slack) <= TOL, kernel
 
 

@@ -52,6 +52,7 @@ struct das_plan_s {
     RxPos *d_rx = nullptr;
     void *d_perm = nullptr;
     size_t perm_bytes = 0;
+    bool perm_pads_zero = false;   // scratch holds the padded layout with zero pad rows
     // device staging of das_beamform_host
     void *d_rf = nullptr, *d_out = nullptr;
     float *d_tau = nullptr, *d_w = nullptr;
@@ -59,6 +60,7 @@ struct das_plan_s {
 
     size_t elem_bytes() const { return dtype == DAS_C64 ? 8 : 4; }
     size_t rf_bytes() const { return (size_t)B * Q * M * K * elem_bytes(); }
+    size_t padded_bytes() const { return (size_t)B * Q * M * (K + 3) * elem_bytes(); }
     size_t out_bytes() const { return (size_t)B * (size_t)N * elem_bytes(); }
     size_t txw_bytes() const { return (size_t)Q * (size_t)N * sizeof(float); }
 };
@@ -150,7 +152,8 @@ das_status das_plan_create(das_plan *plan, const das_grid *grid, const float *rx
     if (dtype != DAS_F32 && dtype != DAS_C64) return fail(DAS_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
     if (B < 1 || Q < 1 || M < 1 || K < 1) return fail(DAS_ERR_INVALID_ARG, "B, Q, M, K must be >= 1");
     const long long N = (long long)grid->nx * grid->ny * grid->nz;
-    if ((long long)Q * M * K >= (1LL << 31)) return fail(DAS_ERR_INVALID_ARG, "Q*M*K must be < 2^31");
+    if ((long long)Q * M * (K + 3) >= (1LL << 31))
+        return fail(DAS_ERR_INVALID_ARG, "Q*M*(K+3) must be < 2^31");
     if (N * B >= (1LL << 31)) return fail(DAS_ERR_INVALID_ARG, "B*N must be < 2^31");
     if ((long long)Q * N >= (1LL << 40)) return fail(DAS_ERR_INVALID_ARG, "Q*N too large");
     if (K >= (1 << 22)) return fail(DAS_ERR_INVALID_ARG, "K must be < 2^22");
@@ -276,20 +279,30 @@ das_status das_beamform(das_plan p, const void *rf, const float *tau_tx, const f
 
     const void *src = rf;
     const bool permute = kernel != DAS_KERNEL_BL;
+    const int layout = kernel == DAS_KERNEL_BI ? 0 : 2;
     if (permute && !p->d_perm) {
-        cudaError_t e = cudaMalloc(&p->d_perm, p->rf_bytes());
+        // sized for the padded layout, which is the larger of the two
+        cudaError_t e = cudaMalloc(&p->d_perm, p->padded_bytes());
         if (e != cudaSuccess) {
             p->d_perm = nullptr;
             cudaGetLastError();
             return cuda_fail(e, "permute scratch allocation");
         }
-        p->perm_bytes = p->rf_bytes();
+        p->perm_bytes = p->padded_bytes();
+        p->perm_pads_zero = false;
     }
+    if (permute && layout == 2 && !p->perm_pads_zero) {
+        // the pad rows are never written by the permute, so zeroing once suffices
+        cudaError_t e = cudaMemsetAsync(p->d_perm, 0, p->padded_bytes(), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "zeroing the permute scratch");
+        p->perm_pads_zero = true;
+    }
+    if (permute && layout == 0) p->perm_pads_zero = false;
     cudaError_t e = cudaSuccess;
     if (p->timing) e = cudaEventRecord(p->ev[0], stream);
     if (e == cudaSuccess && permute) {
         e = das::launch_permute(rf, p->d_perm, (int)p->elem_bytes(), p->B, p->Q, p->M, p->K,
-                                kernel == DAS_KERNEL_BI ? 0 : 1, p->num_sms, stream);
+                                layout, p->num_sms, stream);
         src = p->d_perm;
     }
     if (e == cudaSuccess && p->timing) e = cudaEventRecord(p->ev[1], stream);
@@ -382,12 +395,13 @@ das_status das_permute(const void *in, void *out, das_dtype dtype, int B, int Q,
     if (dtype != DAS_F32 && dtype != DAS_C64) return fail(DAS_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
     if (B < 1 || Q < 1 || M < 1 || K < 1) return fail(DAS_ERR_INVALID_ARG, "B, Q, M, K must be >= 1");
     if ((long long)Q * M >= (1LL << 31)) return fail(DAS_ERR_INVALID_ARG, "Q*M must be < 2^31");
-    if (layout != 0 && layout != 1) return fail(DAS_ERR_INVALID_ARG, "layout must be 0 or 1");
+    if (layout < 0 || layout > 2) return fail(DAS_ERR_INVALID_ARG, "layout must be 0, 1 or 2");
     const size_t eb = dtype == DAS_C64 ? 8 : 4;
     const size_t bytes = (size_t)B * Q * M * K * eb;
+    const size_t obytes = (size_t)B * Q * M * (K + (layout == 2 ? 3 : 0)) * eb;
     const char *a = static_cast<const char *>(in);
     const char *b = static_cast<const char *>(out);
-    if (a < b + bytes && b < a + bytes) return fail(DAS_ERR_INVALID_ARG, "in and out overlap");
+    if (a < b + obytes && b < a + bytes) return fail(DAS_ERR_INVALID_ARG, "in and out overlap");
     int dev = 0, sms = 1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

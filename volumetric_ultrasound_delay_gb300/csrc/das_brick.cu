@@ -6,24 +6,41 @@
 // walking the same (q, m) at the same time hit the same L1 lines; bricks are
 // flat in z because one voxel step in depth moves the delay by many samples.
 //
-// The record is permuted to Q x M x K x B, so the two rows a voxel reads for a
-// (q, m) are adjacent 16 * G * J-byte runs.  A group of G lanes owns one voxel;
-// lane t loads the 16-byte chunks t, t + G, ... of both rows (G = 8: one full
-// 128-byte line per row and instruction).
+// The record is permuted to the zero-padded layout Q x M x (K+3) x B (sample k
+// of slab (q, m) at row k + 1, rows 0, K+1, K+2 zero), so the two rows a voxel
+// reads for a (q, m) are adjacent 16 * G * J-byte runs and a pair that hangs
+// over either end of the record reads a zero row instead of needing special
+// weights.  A group of G lanes owns one voxel; lane t loads the 16-byte chunks
+// t, t + G, ... of both rows (G = 8: one full 128-byte line per row).
 //
 // Geometry is computed once per (voxel, transmit, receiver) instead of once per
 // lane, and staged in shared memory:
 //   phase A (per block of 32 receivers): distance |x_v - r_m| in samples and the
 //            F-number test for all V voxels (warp = voxel, lane = receiver); a
 //            CTA-wide bit mask keeps only receivers inside the aperture of at
-//            least one voxel of the brick, so whole receiver blocks outside
-//            every aperture cost nothing;
-//   phase B (per transmit): row index and the two interpolation weights (IQ:
-//            phase-rotated complex weights) of every active (voxel, receiver),
-//            double-buffered so one barrier per transmit suffices;
-//   phase C: every group walks the active receivers, reading its entry with a
-//            broadcast shared-memory load and accumulating 2 rows x its chunks.
+//            least one voxel of the brick, so receivers outside every aperture
+//            of the brick cost nothing;
+//   phase B (per transmit): an 8-byte entry {row, fraction} (IQ: 16 bytes, plus
+//            the demodulation phase) for every (voxel, receiver) pair that
+//            contributes, i.e. inside that voxel's aperture with a sample inside
+//            the record.  A warp ballot compacts each voxel's entries into a
+//            dense list (warp = voxel, lane = receiver), so no later step spends
+//            work on pairs that add nothing.  Entries are double-buffered, so one
+//            barrier per transmit suffices, and the per-voxel lists are padded so
+//            the groups of a warp read different shared-memory banks;
+//   phase C: every group walks its own voxel's list U entries at a time: the
+//            entries, then all 2 J U row loads, then the FMAs, so each warp keeps
+//            several loads in flight; the groups of a warp run independently.
 #include "das_device.cuh"
+
+// tuning: receivers per phase-C trip when a lane holds one chunk (J = 1), and
+// the CTAs per SM the register allocation must allow
+#ifndef DAS_BRICK_U1
+#define DAS_BRICK_U1 2
+#endif
+#ifndef DAS_BRICK_MIN_BLOCKS
+#define DAS_BRICK_MIN_BLOCKS 5
+#endif
 
 namespace das {
 namespace {
@@ -33,30 +50,57 @@ constexpr int WARPS = THREADS / 32;
 constexpr int MC = 32;                 // receivers per block (one per lane in phase A/B)
 constexpr float FAR = 1.0e30f;         // distance marking "outside the aperture"
 
+// brick footprint in x (voxels); the footprint in y is V / BX
 template <int V>
 struct BrickShape {
     static constexpr int BX = V >= 128 ? 16 : (V >= 32 ? 8 : 4);
-    static constexpr int BY = V / BX;
 };
 
+// {row as int bits, fraction} or, for IQ, {row, fraction, cos, sin}
 template <bool CPLX>
-struct Weights;
-template <>
-struct Weights<false> { using type = float2; };    // (w0, w1)
-template <>
-struct Weights<true> { using type = float4; };     // (W0.re, W0.im, W1.re, W1.im)
+using Entry = typename std::conditional<CPLX, float4, float2>::type;
+
+// entries per voxel list: MC plus padding, chosen so a list starts on a
+// 16-byte boundary and consecutive voxels start 4 banks apart
+template <bool CPLX>
+constexpr int entry_stride() { return CPLX ? MC + 1 : MC + 2; }
 
 template <int G, bool CPLX>
 size_t smem_bytes(int Q)
 {
     constexpr int V = WARPS * (32 / G);
-    using W = typename Weights<CPLX>::type;
-    return sizeof(W) * 2 * V * MC + sizeof(int) * 2 * V * MC + sizeof(float) * V * MC +
-           sizeof(float2) * (size_t)V * Q + sizeof(unsigned) * 2 * WARPS;
+    return sizeof(Entry<CPLX>) * 2 * V * entry_stride<CPLX>() + sizeof(float) * V * MC +
+           sizeof(float2) * (size_t)V * Q + sizeof(int) * 2 * V + sizeof(unsigned) * 2 * WARPS;
+}
+
+// acc[c][.] += w0 * s0[c] + w1 * s1[c], w1 = wq * fraction, w0 = wq - w1
+// (IQ: both weights rotated by the entry's phase)
+template <int J, bool CPLX, typename T, typename E>
+__device__ __forceinline__ void accumulate(T (&acc)[J][CPLX ? 2 : 4], float wq, const E &e,
+                                           const float4 (&s0)[J], const float4 (&s1)[J])
+{
+    const float w1 = wq * e.y;
+    const float w0 = wq - w1;
+#pragma unroll
+    for (int c = 0; c < J; ++c) {
+        if constexpr (CPLX) {
+            const float2 W0 = make_float2(w0 * e.z, w0 * e.w);
+            const float2 W1 = make_float2(w1 * e.z, w1 * e.w);
+            cfma(acc[c][0], W0, make_float2(s0[c].x, s0[c].y));
+            cfma(acc[c][1], W0, make_float2(s0[c].z, s0[c].w));
+            cfma(acc[c][0], W1, make_float2(s1[c].x, s1[c].y));
+            cfma(acc[c][1], W1, make_float2(s1[c].z, s1[c].w));
+        } else {
+            acc[c][0] = fmaf(w0, s0[c].x, fmaf(w1, s1[c].x, acc[c][0]));
+            acc[c][1] = fmaf(w0, s0[c].y, fmaf(w1, s1[c].y, acc[c][1]));
+            acc[c][2] = fmaf(w0, s0[c].z, fmaf(w1, s1[c].z, acc[c][2]));
+            acc[c][3] = fmaf(w0, s0[c].w, fmaf(w1, s1[c].w, acc[c][3]));
+        }
+    }
 }
 
 template <int G, int J, bool CPLX>
-__global__ void __launch_bounds__(THREADS, 4)
+__global__ void __launch_bounds__(THREADS, DAS_BRICK_MIN_BLOCKS)
 das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__ perm,
                  const float *__restrict__ tau, const float *__restrict__ wtx,
                  float *__restrict__ out, int bricks_x, int bricks_y)
@@ -65,15 +109,18 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restric
     constexpr int V = WARPS * NW;                  // voxels per CTA
     constexpr int BX = BrickShape<V>::BX;
     constexpr int CH = CPLX ? 2 : 4;               // elements per 16-byte chunk
+    constexpr int U = J >= 4 ? 1 : (J == 2 ? 2 : DAS_BRICK_U1);   // receivers per loop trip
     using T = typename std::conditional<CPLX, float2, float>::type;
-    using W = typename Weights<CPLX>::type;
+    using E = Entry<CPLX>;
+    constexpr int ES = entry_stride<CPLX>();
+    constexpr int ROWB = 16 * G * J;               // bytes of one row (B * element size)
 
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    W *wts = reinterpret_cast<W *>(smem_raw);                        // [2][V][MC]
-    int *rows = reinterpret_cast<int *>(wts + 2 * V * MC);           // [2][V][MC]
-    float *dist = reinterpret_cast<float *>(rows + 2 * V * MC);      // [V][MC]
-    float2 *tx = reinterpret_cast<float2 *>(dist + V * MC);          // [V][Q]  (tau*fs - t0*fs, w)
-    unsigned *masks = reinterpret_cast<unsigned *>(tx + V * g.Q);    // [2][WARPS]
+    E *ent = reinterpret_cast<E *>(smem_raw);                        // [2][V][ES]
+    float *dist = reinterpret_cast<float *>(ent + 2 * V * ES);       // [V][MC]
+    float2 *tx = reinterpret_cast<float2 *>(dist + V * MC);          // [V][Q] (tau*fs - t0*fs, w)
+    int *cnt = reinterpret_cast<int *>(tx + V * g.Q);                // [2][V] list lengths
+    unsigned *masks = reinterpret_cast<unsigned *>(cnt + 2 * V);     // [2][WARPS]
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -82,6 +129,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restric
     const int rb = blockIdx.x / bricks_x;
     const int by = rb % bricks_y;
     const int iz = rb / bricks_y;
+    const int KP = g.K + 3;                        // rows per padded slab
 
     // ---- per-voxel transmit delay (samples) and weight, once per CTA
     for (int e = tid; e < V * g.Q; e += THREADS) {
@@ -102,7 +150,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restric
     const int cv = warp * NW + grp;
     const int cix = bx * BX + cv % BX, ciy = by * (V / BX) + cv / BX;
     const bool cvalid = cix < g.nx && ciy < g.ny;
-    const T *permT = reinterpret_cast<const T *>(perm);
+    const char *permB = reinterpret_cast<const char *>(perm) + t * 16;
 
     T acc[J][CH];
 #pragma unroll
@@ -140,58 +188,77 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restric
 
         for (int q = 0; q < g.Q; ++q) {
             const int buf = q & 1;
-            // ---- phase B: row and weights of every active (voxel, receiver)
-            if ((mask >> lane) & 1u) {
-                const int rowbase = (q * g.M + m0 + lane) * g.K;
+            // ---- phase B: compacted {row, fraction (, phase)} lists, warp = voxel
+            {
+                const bool active = (mask >> lane) & 1u;
+                const int slab = (q * g.M + m0 + lane) * KP;
+                const unsigned below = (1u << lane) - 1u;
                 for (int v = warp; v < V; v += WARPS) {
-                    const float2 tw = tx[v * g.Q + q];
-                    const float f = tw.x + dist[v * MC + lane];
-                    int r0;
-                    float w0, w1;
-                    const bool nz = sample_pair(f, tw.y, g.K, r0, w0, w1);
-                    const int idx = (buf * V + v) * MC + lane;
-                    rows[idx] = rowbase + r0;
-                    if constexpr (CPLX) {
-                        const float2 ph = nz ? demod_phase(g, f) : make_float2(1.f, 0.f);
-                        wts[idx] = make_float4(w0 * ph.x, w0 * ph.y, w1 * ph.x, w1 * ph.y);
-                    } else {
-                        wts[idx] = make_float2(w0, w1);
+                    const float f = tx[v * g.Q + q].x + dist[v * MC + lane];
+                    const float fl = floorf(f);
+                    // inside the aperture (dist < FAR) and a sample inside the record;
+                    // false for NaN / inf
+                    const bool ok = active && (fl >= -1.f) && (fl <= (float)(g.K - 1));
+                    const unsigned bal = __ballot_sync(0xffffffffu, ok);
+                    if (ok) {
+                        const int row = slab + (int)fl + 1;
+                        const float a = f - fl;
+                        E e;
+                        if constexpr (CPLX) {
+                            const float2 ph = demod_phase(g, f);
+                            e = make_float4(__int_as_float(row), a, ph.x, ph.y);
+                        } else {
+                            e = make_float2(__int_as_float(row), a);
+                        }
+                        ent[(buf * V + v) * ES + __popc(bal & below)] = e;
                     }
+                    if (lane == 0) cnt[buf * V + v] = __popc(bal);
                 }
             }
             __syncthreads();
 
-            // ---- phase C: accumulate
-            const W *wv = wts + (buf * V + cv) * MC;
-            const int *rv = rows + (buf * V + cv) * MC;
-            unsigned mm = mask;
-            while (mm) {
-                const int j = __ffs(mm) - 1;
-                mm &= mm - 1u;
-                const W ww = wv[j];
-                bool zero;
-                if constexpr (CPLX) zero = ww.x == 0.f && ww.y == 0.f && ww.z == 0.f && ww.w == 0.f;
-                else zero = ww.x == 0.f && ww.y == 0.f;
-                if (zero) continue;                // uniform within the group
-                const T *p0 = permT + (long long)rv[j] * g.B + t * CH;
-                const T *p1 = p0 + g.B;
+            // ---- phase C: accumulate this group's list, U entries per trip
+            const float wq = tx[cv * g.Q + q].y;
+            const E *ev = ent + (buf * V + cv) * ES;
+            const int n_ent = cnt[buf * V + cv];
+            int i = 0;
+            for (; i + U <= n_ent; i += U) {
+                E e[U];
+                if constexpr (!CPLX && U % 2 == 0) {
+                    // two 8-byte entries per 16-byte shared load
 #pragma unroll
-                for (int c = 0; c < J; ++c) {
-                    const float4 u0 = __ldg(reinterpret_cast<const float4 *>(p0 + c * G * CH));
-                    const float4 u1 = __ldg(reinterpret_cast<const float4 *>(p1 + c * G * CH));
-                    if constexpr (CPLX) {
-                        const float2 W0 = make_float2(ww.x, ww.y), W1 = make_float2(ww.z, ww.w);
-                        cfma(acc[c][0], W0, make_float2(u0.x, u0.y));
-                        cfma(acc[c][1], W0, make_float2(u0.z, u0.w));
-                        cfma(acc[c][0], W1, make_float2(u1.x, u1.y));
-                        cfma(acc[c][1], W1, make_float2(u1.z, u1.w));
-                    } else {
-                        acc[c][0] = fmaf(ww.x, u0.x, fmaf(ww.y, u1.x, acc[c][0]));
-                        acc[c][1] = fmaf(ww.x, u0.y, fmaf(ww.y, u1.y, acc[c][1]));
-                        acc[c][2] = fmaf(ww.x, u0.z, fmaf(ww.y, u1.z, acc[c][2]));
-                        acc[c][3] = fmaf(ww.x, u0.w, fmaf(ww.y, u1.w, acc[c][3]));
+                    for (int u = 0; u < U; u += 2) {
+                        const float4 two = *reinterpret_cast<const float4 *>(ev + i + u);
+                        e[u] = make_float2(two.x, two.y);
+                        e[u + 1] = make_float2(two.z, two.w);
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < U; ++u) e[u] = ev[i + u];
+                }
+                float4 s0[U][J], s1[U][J];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const char *p0 = permB + (long long)__float_as_int(e[u].x) * ROWB;
+#pragma unroll
+                    for (int c = 0; c < J; ++c) {
+                        s0[u][c] = __ldg(reinterpret_cast<const float4 *>(p0 + c * G * 16));
+                        s1[u][c] = __ldg(reinterpret_cast<const float4 *>(p0 + ROWB + c * G * 16));
                     }
                 }
+#pragma unroll
+                for (int u = 0; u < U; ++u) accumulate<J, CPLX>(acc, wq, e[u], s0[u], s1[u]);
+            }
+            for (; i < n_ent; ++i) {
+                const E e = ev[i];
+                float4 s0[J], s1[J];
+                const char *p0 = permB + (long long)__float_as_int(e.x) * ROWB;
+#pragma unroll
+                for (int c = 0; c < J; ++c) {
+                    s0[c] = __ldg(reinterpret_cast<const float4 *>(p0 + c * G * 16));
+                    s1[c] = __ldg(reinterpret_cast<const float4 *>(p0 + ROWB + c * G * 16));
+                }
+                accumulate<J, CPLX>(acc, wq, e, s0, s1);
             }
         }
     }
@@ -210,7 +277,8 @@ cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, cons
                        const float *w, void *out, cudaStream_t stream)
 {
     constexpr int V = WARPS * (32 / G);
-    constexpr int BX = BrickShape<V>::BX, BY = V / BX;
+    constexpr int BX = BrickShape<V>::BX;
+    constexpr int BY = V / BX;
     const int bricks_x = (g.nx + BX - 1) / BX;
     const int bricks_y = (g.ny + BY - 1) / BY;
     const long long blocks = (long long)bricks_x * bricks_y * g.nz;

@@ -9,8 +9,11 @@
 // padding per row, so the scalar shared-memory traffic is conflict-free for
 // 4-byte elements.  The copy moves opaque element values and is bit-exact.
 //
-//   layout 0: out[((k*Q + q)*M + m)*B + b]   (K x Q x M x B)
-//   layout 1: out[((q*M + m)*K + k)*B + b]   (Q x M x K x B)
+//   layout 0: out[((k*Q + q)*M + m)*B + b]         (K x Q x M x B)
+//   layout 1: out[((q*M + m)*K + k)*B + b]         (Q x M x K x B)
+//   layout 2: out[((q*M + m)*(K+3) + k + 1)*B + b] (Q x M x (K+3) x B: every
+//             (q, m) slab has a row before k = 0 and two rows after k = K-1
+//             that this kernel never writes; the brick kernel keeps them zero)
 #include <cstdint>
 #include <cstring>
 
@@ -106,7 +109,9 @@ cudaError_t launch_typed(const void *in, void *out, int B, int Q, int M, int K, 
     constexpr int V = 16 / sizeof(T);
     const int QM = Q * M;
     const long long osk = layout == 0 ? (long long)QM * B : (long long)B;
-    const long long osqm = layout == 0 ? (long long)B : (long long)K * B;
+    const long long osqm = layout == 0 ? (long long)B
+                         : layout == 1 ? (long long)K * B : (long long)(K + 3) * B;
+    if (layout == 2) out = static_cast<T *>(out) + B;   // row k = 0 of slab 0
     const int blocks_b = (B + TILE - 1) / TILE;
     const int blocks_k = (K + TILE * SUB - 1) / (TILE * SUB);
     const long long n_blocks = (long long)QM * blocks_b * blocks_k;

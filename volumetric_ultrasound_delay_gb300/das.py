@@ -208,12 +208,14 @@ class Plan:
 
 
 def permute(rf, out, layout: int = 0, stream=None):
-    """Bit-exact B x Q x M x K -> K x Q x M x B (layout 0) or Q x M x K x B (layout 1)."""
+    """Bit-exact B x Q x M x K -> K x Q x M x B (layout 0), Q x M x K x B (layout 1)
+    or Q x M x (K+3) x B with sample k at row k + 1 and pad rows untouched (layout 2)."""
     import torch
     if rf.dtype not in (torch.float32, torch.complex64) or rf.dim() != 4:
         raise TypeError("rf must be a 4-D float32 or complex64 CUDA tensor")
     B, Q, M, K = rf.shape
     dt = DAS_C64 if rf.dtype == torch.complex64 else DAS_F32
-    _check(lib().das_permute(_dev_ptr(rf, "rf"), _dev_ptr(out, "out", rf.dtype, rf.numel()), dt,
+    n_out = B * Q * M * (K + 3 if layout == 2 else K)
+    _check(lib().das_permute(_dev_ptr(rf, "rf"), _dev_ptr(out, "out", rf.dtype, n_out), dt,
                              B, Q, M, K, layout, _stream_handle(stream)))
     return out
