@@ -3,7 +3,7 @@
 // Each CTA (8 warps) owns a brick of V voxels in one x-y slice (8 x 4 for 32
 // frames of float32) and all B frames of them.  Neighbouring voxels of a slice
 // need nearly the same sample rows of every receiver, so the warps of a CTA
-// walking the same (q, m) at the same time hit the same L1 lines; bricks are
+// walking the same receivers at the same time hit the same L1 lines; bricks are
 // flat in z because one voxel step in depth moves the delay by many samples.
 //
 // The record is permuted to the zero-padded layout Q x M x (K+3) x B (sample k
@@ -13,47 +13,52 @@
 // weights.  A group of G lanes owns one voxel; lane t loads the 16-byte chunks
 // t, t + G, ... of both rows (G = 8: one full 128-byte line per row).
 //
-// Geometry is computed once per (voxel, transmit, receiver) instead of once per
-// lane, and staged in shared memory:
-//   phase A (per block of 32 receivers): distance |x_v - r_m| in samples and the
-//            F-number test for all V voxels (warp = voxel, lane = receiver); a
-//            CTA-wide bit mask keeps only receivers inside the aperture of at
-//            least one voxel of the brick, so receivers outside every aperture
-//            of the brick cost nothing;
-//   phase B (per transmit): an 8-byte entry {row, fraction} (IQ: 16 bytes, plus
-//            the demodulation phase) for every (voxel, receiver) pair that
-//            contributes, i.e. inside that voxel's aperture with a sample inside
-//            the record.  A warp ballot compacts each voxel's entries into a
-//            dense list (warp = voxel, lane = receiver), so no later step spends
-//            work on pairs that add nothing.  Entries are double-buffered, so one
-//            barrier per transmit suffices, and the per-voxel lists are padded so
-//            the groups of a warp read different shared-memory banks;
-//   phase C: every group walks its own voxel's list U entries at a time: the
-//            entries, then all 2 J U row loads, then the FMAs, so each warp keeps
-//            several loads in flight; the groups of a warp run independently.
+// A warp owns NW = 32 / G voxels and does all the work for them itself, so
+// after the per-CTA preload of transmit delays no step needs a CTA barrier:
+//   phase A (per block of 32 receivers, lane = receiver): distance |x_v - r_m|
+//            in samples and the F-number test for the warp's NW voxels, kept in
+//            registers; a block whose receivers lie outside every aperture of
+//            the warp's voxels is skipped;
+//   phase B (per transmit, lane = receiver): an 8-byte entry {row, fraction}
+//            (IQ: 16 bytes, plus the demodulation phase) for every pair that
+//            contributes (inside the voxel's aperture, a sample inside the
+//            record); a warp ballot compacts each voxel's entries into a dense
+//            list in the warp's own shared memory, and the list lengths stay in
+//            registers.  Lists are double-buffered by transmit parity;
+//   phase C: each group walks its voxel's list U entries per trip (entries,
+//            then all 2 J U row loads, then the FMAs), independently of the
+//            other groups of the warp.
 #include "das_device.cuh"
 
-// tuning: receivers per phase-C trip when a lane holds one chunk (J = 1), and
-// the CTAs per SM the register allocation must allow
+// tuning: receivers per phase-C trip when a lane holds one chunk (J = 1), the
+// CTAs per SM the register allocation must allow, and whether the warps of a
+// CTA meet at a barrier after every block of receivers
 #ifndef DAS_BRICK_U1
 #define DAS_BRICK_U1 2
 #endif
 #ifndef DAS_BRICK_MIN_BLOCKS
 #define DAS_BRICK_MIN_BLOCKS 5
 #endif
+#ifndef DAS_BRICK_CHUNK_BARRIER
+#define DAS_BRICK_CHUNK_BARRIER 0
+#endif
+#ifndef DAS_BRICK_WARPS
+#define DAS_BRICK_WARPS 8
+#endif
 
 namespace das {
 namespace {
 
-constexpr int THREADS = 256;
-constexpr int WARPS = THREADS / 32;
-constexpr int MC = 32;                 // receivers per block (one per lane in phase A/B)
+constexpr int WARPS = DAS_BRICK_WARPS;   // warps per CTA (= per brick)
+constexpr int THREADS = 32 * WARPS;
+constexpr int MC = 32;                 // receivers per block (one per lane in phases A and B)
 constexpr float FAR = 1.0e30f;         // distance marking "outside the aperture"
 
-// brick footprint in x (voxels); the footprint in y is V / BX
+// brick footprint in x (voxels), as square as powers of two allow; the
+// footprint in y is V / BX
 template <int V>
 struct BrickShape {
-    static constexpr int BX = V >= 128 ? 16 : (V >= 32 ? 8 : 4);
+    static constexpr int BX = V >= 512 ? 32 : (V >= 128 ? 16 : (V >= 32 ? 8 : 4));
 };
 
 // {row as int bits, fraction} or, for IQ, {row, fraction, cos, sin}
@@ -69,8 +74,7 @@ template <int G, bool CPLX>
 size_t smem_bytes(int Q)
 {
     constexpr int V = WARPS * (32 / G);
-    return sizeof(Entry<CPLX>) * 2 * V * entry_stride<CPLX>() + sizeof(float) * V * MC +
-           sizeof(float2) * (size_t)V * Q + sizeof(int) * 2 * V + sizeof(unsigned) * 2 * WARPS;
+    return sizeof(Entry<CPLX>) * 2 * V * entry_stride<CPLX>() + sizeof(float2) * (size_t)V * Q;
 }
 
 // acc[c][.] += w0 * s0[c] + w1 * s1[c], w1 = wq * fraction, w0 = wq - w1
@@ -110,21 +114,18 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restric
     constexpr int BX = BrickShape<V>::BX;
     constexpr int CH = CPLX ? 2 : 4;               // elements per 16-byte chunk
     constexpr int U = J >= 4 ? 1 : (J == 2 ? 2 : DAS_BRICK_U1);   // receivers per loop trip
-    using T = typename std::conditional<CPLX, float2, float>::type;
-    using E = Entry<CPLX>;
     constexpr int ES = entry_stride<CPLX>();
     constexpr int ROWB = 16 * G * J;               // bytes of one row (B * element size)
+    using T = typename std::conditional<CPLX, float2, float>::type;
+    using E = Entry<CPLX>;
 
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    E *ent = reinterpret_cast<E *>(smem_raw);                        // [2][V][ES]
-    float *dist = reinterpret_cast<float *>(ent + 2 * V * ES);       // [V][MC]
-    float2 *tx = reinterpret_cast<float2 *>(dist + V * MC);          // [V][Q] (tau*fs - t0*fs, w)
-    int *cnt = reinterpret_cast<int *>(tx + V * g.Q);                // [2][V] list lengths
-    unsigned *masks = reinterpret_cast<unsigned *>(cnt + 2 * V);     // [2][WARPS]
-
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
+    E *ent = reinterpret_cast<E *>(smem_raw) + warp * (2 * NW * ES);        // this warp's [2][NW][ES]
+    float2 *tx = reinterpret_cast<float2 *>(reinterpret_cast<E *>(smem_raw) + 2 * V * ES);  // [V][Q]
+
     const int bx = blockIdx.x % bricks_x;
     const int rb = blockIdx.x / bricks_x;
     const int by = rb % bricks_y;
@@ -143,14 +144,14 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restric
         }
         tx[e] = val;
     }
+    __syncthreads();
 
-    // ---- consumer identity: group grp of this warp owns voxel cv
+    // ---- this warp's voxels v0 + i, i < NW; group grp consumes voxel v0 + grp
+    const int v0 = warp * NW;
     const int grp = lane / G;
     const int t = lane % G;
-    const int cv = warp * NW + grp;
-    const int cix = bx * BX + cv % BX, ciy = by * (V / BX) + cv / BX;
-    const bool cvalid = cix < g.nx && ciy < g.ny;
     const char *permB = reinterpret_cast<const char *>(perm) + t * 16;
+    const unsigned below = (1u << lane) - 1u;
 
     T acc[J][CH];
 #pragma unroll
@@ -158,47 +159,38 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restric
 #pragma unroll
         for (int e = 0; e < CH; ++e) acc[c][e] = T{};
 
-    __syncthreads();
-
-    int chunk = 0;
-    for (int m0 = 0; m0 < g.M; m0 += MC, ++chunk) {
-        // ---- phase A: distances and aperture, warp = voxel, lane = receiver
-        unsigned any = 0;
+    for (int m0 = 0; m0 < g.M; m0 += MC) {
+        // ---- phase A: distances of the warp's voxels to receiver m0 + lane
         const int m = m0 + lane;
         const RxPos r = m < g.M ? __ldg(rx + m) : make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int v = warp; v < V; v += WARPS) {
+        float dist[NW];
+        bool any = false;
+#pragma unroll
+        for (int i = 0; i < NW; ++i) {
+            const int v = v0 + i;
             const int ix = bx * BX + v % BX, iy = by * (V / BX) + v / BX;
-            float d = FAR;
+            dist[i] = FAR;
             if (m < g.M && ix < g.nx && iy < g.ny) {
-                float dd;
-                if (receive_geometry(g, voxel_position(g, ix, iy, iz), r, dd)) {
-                    d = dd;
-                    any = 1u;
+                float d;
+                if (receive_geometry(g, voxel_position(g, ix, iy, iz), r, d)) {
+                    dist[i] = d;
+                    any = true;
                 }
             }
-            dist[v * MC + lane] = d;
         }
-        const unsigned bal = __ballot_sync(0xffffffffu, any);
-        if (lane == 0) masks[(chunk & 1) * WARPS + warp] = bal;
-        __syncthreads();
-        unsigned mask = 0;
+        if (__ballot_sync(0xffffffffu, any) != 0u) {
+            for (int q = 0; q < g.Q; ++q) {
+                E *eb = ent + (q & 1) * NW * ES;
+                // ---- phase B: compacted entry lists of the warp's voxels
+                int n_mine = 0;
+                const int slab = (q * g.M + m) * KP;
 #pragma unroll
-        for (int w = 0; w < WARPS; ++w) mask |= masks[(chunk & 1) * WARPS + w];
-        if (mask == 0u) continue;                  // CTA-uniform
-
-        for (int q = 0; q < g.Q; ++q) {
-            const int buf = q & 1;
-            // ---- phase B: compacted {row, fraction (, phase)} lists, warp = voxel
-            {
-                const bool active = (mask >> lane) & 1u;
-                const int slab = (q * g.M + m0 + lane) * KP;
-                const unsigned below = (1u << lane) - 1u;
-                for (int v = warp; v < V; v += WARPS) {
-                    const float f = tx[v * g.Q + q].x + dist[v * MC + lane];
+                for (int i = 0; i < NW; ++i) {
+                    const float f = tx[(v0 + i) * g.Q + q].x + dist[i];
                     const float fl = floorf(f);
-                    // inside the aperture (dist < FAR) and a sample inside the record;
-                    // false for NaN / inf
-                    const bool ok = active && (fl >= -1.f) && (fl <= (float)(g.K - 1));
+                    // inside the aperture (dist < FAR) and a sample inside the
+                    // record; false for NaN / inf
+                    const bool ok = (fl >= -1.f) && (fl <= (float)(g.K - 1));
                     const unsigned bal = __ballot_sync(0xffffffffu, ok);
                     if (ok) {
                         const int row = slab + (int)fl + 1;
@@ -210,60 +202,66 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restric
                         } else {
                             e = make_float2(__int_as_float(row), a);
                         }
-                        ent[(buf * V + v) * ES + __popc(bal & below)] = e;
+                        eb[i * ES + __popc(bal & below)] = e;
                     }
-                    if (lane == 0) cnt[buf * V + v] = __popc(bal);
+                    if (i == grp) n_mine = __popc(bal);
                 }
-            }
-            __syncthreads();
+                __syncwarp();
 
-            // ---- phase C: accumulate this group's list, U entries per trip
-            const float wq = tx[cv * g.Q + q].y;
-            const E *ev = ent + (buf * V + cv) * ES;
-            const int n_ent = cnt[buf * V + cv];
-            int i = 0;
-            for (; i + U <= n_ent; i += U) {
-                E e[U];
-                if constexpr (!CPLX && U % 2 == 0) {
-                    // two 8-byte entries per 16-byte shared load
+                // ---- phase C: this group's list, U entries per trip
+                const float wq = tx[(v0 + grp) * g.Q + q].y;
+                const E *ev = eb + grp * ES;
+                int i = 0;
+                for (; i + U <= n_mine; i += U) {
+                    E e[U];
+                    if constexpr (!CPLX && U % 2 == 0) {
+                        // two 8-byte entries per 16-byte shared load
 #pragma unroll
-                    for (int u = 0; u < U; u += 2) {
-                        const float4 two = *reinterpret_cast<const float4 *>(ev + i + u);
-                        e[u] = make_float2(two.x, two.y);
-                        e[u + 1] = make_float2(two.z, two.w);
+                        for (int u = 0; u < U; u += 2) {
+                            const float4 two = *reinterpret_cast<const float4 *>(ev + i + u);
+                            e[u] = make_float2(two.x, two.y);
+                            e[u + 1] = make_float2(two.z, two.w);
+                        }
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < U; ++u) e[u] = ev[i + u];
                     }
-                } else {
+                    float4 s0[U][J], s1[U][J];
 #pragma unroll
-                    for (int u = 0; u < U; ++u) e[u] = ev[i + u];
+                    for (int u = 0; u < U; ++u) {
+                        const char *p0 = permB + (long long)__float_as_int(e[u].x) * ROWB;
+#pragma unroll
+                        for (int c = 0; c < J; ++c) {
+                            s0[u][c] = __ldg(reinterpret_cast<const float4 *>(p0 + c * G * 16));
+                            s1[u][c] = __ldg(reinterpret_cast<const float4 *>(p0 + ROWB + c * G * 16));
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < U; ++u) accumulate<J, CPLX>(acc, wq, e[u], s0[u], s1[u]);
                 }
-                float4 s0[U][J], s1[U][J];
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const char *p0 = permB + (long long)__float_as_int(e[u].x) * ROWB;
+                for (; i < n_mine; ++i) {
+                    const E e = ev[i];
+                    float4 s0[J], s1[J];
+                    const char *p0 = permB + (long long)__float_as_int(e.x) * ROWB;
 #pragma unroll
                     for (int c = 0; c < J; ++c) {
-                        s0[u][c] = __ldg(reinterpret_cast<const float4 *>(p0 + c * G * 16));
-                        s1[u][c] = __ldg(reinterpret_cast<const float4 *>(p0 + ROWB + c * G * 16));
+                        s0[c] = __ldg(reinterpret_cast<const float4 *>(p0 + c * G * 16));
+                        s1[c] = __ldg(reinterpret_cast<const float4 *>(p0 + ROWB + c * G * 16));
                     }
+                    accumulate<J, CPLX>(acc, wq, e, s0, s1);
                 }
-#pragma unroll
-                for (int u = 0; u < U; ++u) accumulate<J, CPLX>(acc, wq, e[u], s0[u], s1[u]);
-            }
-            for (; i < n_ent; ++i) {
-                const E e = ev[i];
-                float4 s0[J], s1[J];
-                const char *p0 = permB + (long long)__float_as_int(e.x) * ROWB;
-#pragma unroll
-                for (int c = 0; c < J; ++c) {
-                    s0[c] = __ldg(reinterpret_cast<const float4 *>(p0 + c * G * 16));
-                    s1[c] = __ldg(reinterpret_cast<const float4 *>(p0 + ROWB + c * G * 16));
-                }
-                accumulate<J, CPLX>(acc, wq, e, s0, s1);
+                // the next transmit writes the other buffer; the one after that
+                // comes after the next __syncwarp
             }
         }
+#if DAS_BRICK_CHUNK_BARRIER
+        __syncthreads();
+#endif
     }
 
-    if (!cvalid) return;
+    const int cv = v0 + grp;
+    const int cix = bx * BX + cv % BX, ciy = by * (V / BX) + cv / BX;
+    if (cix >= g.nx || ciy >= g.ny) return;
     const long long n = cix + (long long)g.nx * (ciy + (long long)g.ny * iz);
     T *outT = reinterpret_cast<T *>(out);
 #pragma unroll
