@@ -180,6 +180,47 @@ das_status das_plan_destroy(das_plan plan);
 das_status das_permute(const void *in, void *out, das_dtype dtype, int B, int Q, int M,
                        int K, int layout, cudaStream_t stream);
 
+/*
+ * das_beamform_noalloc -- the same computation as a plan running the brick
+ * kernel, for callers that cannot allocate device memory.  The ffdas pages
+ * have no counterpart to this entry point.
+ *
+ * Who it is for: code that must not call cudaMalloc once it is running, such as
+ * the real-time reconstruction loop of a scanner (cudaMalloc can synchronise the
+ * device and stall acquisition) or a host framework that hands out all device
+ * memory from its own pool at start-up and forbids other allocations.  A plan
+ * allocates, so those callers use this call instead.  It allocates nothing:
+ * no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * Arguments are those of das_plan_create and das_beamform together, except that
+ *   rx_xyz   is a DEVICE pointer (M x 3 float32 receiver positions, metres), and
+ *   f_demod  (Hz, DAS_C64 only; 0 = no rotation) is passed directly.
+ * rf, tau_tx, w_tx and out are device buffers in the layouts of das_beamform.
+ *
+ * Scratch: one file-scope static device array of 64 MiB (67,108,864 bytes)
+ * inside libdas, which every GPU that loads the library's kernels holds until
+ * the process exits.  A call needs 16*M (rounded up to 256) +
+ * B*Q*M*(K+3)*element-size bytes of it; larger requests are rejected with
+ * DAS_ERR_INVALID_ARG and a message naming both sizes, and launch nothing.
+ * Every call shares that one array and leaves its contents behind; the call
+ * itself clears the part that must start at zero.  Calls whose device work
+ * overlaps (unordered streams, or several host threads) race on the array and
+ * give wrong results, so serialise them.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) before launching; make that first call before any
+ * stream capture.
+ *
+ * Errors: DAS_ERR_INVALID_ARG (NULL or misaligned pointers, bad sizes, scratch
+ * too small), DAS_ERR_UNSUPPORTED (B / K the brick kernel cannot serve,
+ * f_demod on real data), DAS_ERR_CUDA.  Asynchronous on `stream`.
+ */
+das_status das_beamform_noalloc(const das_grid *grid, const float *rx_xyz, float c, float fs,
+                                float t0, float fnum, double f_demod, das_dtype dtype,
+                                int B, int Q, int M, int K, const void *rf,
+                                const float *tau_tx, const float *w_tx, void *out,
+                                cudaStream_t stream);
+
 /* Text of the last error raised on the calling thread ("" if none). */
 const char *das_last_error_string(void);
 

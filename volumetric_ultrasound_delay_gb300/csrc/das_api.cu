@@ -34,6 +34,8 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
+void das::record_error(const char *msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+
 struct das_plan_s {
     das_grid grid{};
     float c = 0, fs = 0, t0 = 0, fnum = 0;

@@ -28,6 +28,9 @@ using RxPos = float4;
 
 namespace das {
 
+// Sets the text das_last_error_string() returns on this thread.
+void record_error(const char *msg);
+
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_permute(const void *in, void *out, int elem_bytes, int B, int Q, int M, int K,
                            int layout, int num_sms, cudaStream_t stream);

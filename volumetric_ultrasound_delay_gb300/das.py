@@ -40,6 +40,8 @@ _SIGS = {
     "das_plan_device_bytes": (_I, [_VP, ctypes.POINTER(ctypes.c_size_t)]),
     "das_plan_destroy": (_I, [_VP]),
     "das_permute": (_I, [_VP, _VP, _I, _I, _I, _I, _I, _I, _VP]),
+    "das_beamform_noalloc": (_I, [_VP, _VP, _F, _F, _F, _F, ctypes.c_double, _I, _I, _I, _I, _I,
+                                  _VP, _VP, _VP, _VP, _VP]),
     "das_last_error_string": (ctypes.c_char_p, []),
     "das_version": (ctypes.c_char_p, []),
 }
@@ -218,4 +220,27 @@ def permute(rf, out, layout: int = 0, stream=None):
     n_out = B * Q * M * (K + 3 if layout == 2 else K)
     _check(lib().das_permute(_dev_ptr(rf, "rf"), _dev_ptr(out, "out", rf.dtype, n_out), dt,
                              B, Q, M, K, layout, _stream_handle(stream)))
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def beamform_noalloc(grid, rx_xyz, c, fs, t0, fnum, f_demod, rf, tau_tx, w_tx, out,
+                     stream=None):
+    """das_beamform_noalloc: the brick-kernel beamform without any device
+    allocation, for callers that cannot call cudaMalloc while they run (its
+    scratch is a 64 MiB static array inside libdas; see include/das.h).
+    ``rx_xyz`` is a CUDA tensor (M x 3 float32); rf (B x Q x M x K), tau_tx and
+    w_tx (Q x N) and out (B x N) are CUDA tensors as for :meth:`Plan.beamform`."""
+    import torch
+    B, Q, M, K = rf.shape
+    dt = DAS_C64 if rf.dtype == torch.complex64 else DAS_F32
+    N = int(grid[0]) * int(grid[1]) * int(grid[2])
+    g = _Grid(*[int(v) for v in grid[:3]], *[float(v) for v in grid[3:]])
+    _check(lib().das_beamform_noalloc(
+        ctypes.byref(g), _dev_ptr(rx_xyz, "rx_xyz", torch.float32, M * 3), c, fs, t0, fnum,
+        float(f_demod), dt, B, Q, M, K, _dev_ptr(rf, "rf", rf.dtype),
+        _dev_ptr(tau_tx, "tau_tx", torch.float32, Q * N), _dev_ptr(w_tx, "w_tx", torch.float32, Q * N),
+        _dev_ptr(out, "out", rf.dtype, B * N), _stream_handle(stream)))
     return out
