@@ -19,20 +19,26 @@
 //            in samples and the F-number test for the warp's NW voxels, kept in
 //            registers; a block whose receivers lie outside every aperture of
 //            the warp's voxels is skipped;
-//   phase B (per transmit, lane = receiver): an 8-byte entry {row, fraction}
-//            (IQ: 16 bytes, plus the demodulation phase) for every pair that
+//   phase B (per transmit, lane = receiver): an entry for every pair that
 //            contributes (inside the voxel's aperture, a sample inside the
 //            record); a warp ballot compacts each voxel's entries into a dense
 //            list in the warp's own shared memory, and the list lengths stay in
-//            registers.  Lists are double-buffered by transmit parity;
-//   phase C: each group walks its voxel's list U entries per trip (entries,
-//            then all 2 J U row loads, then the FMAs), independently of the
-//            other groups of the warp.
+//            registers.  Lists are double-buffered by transmit parity.  A real
+//            entry is one 32-bit word: the row relative to the first row of
+//            this block of receivers in the high bits, the interpolation
+//            fraction in the low FB bits (FB >= 10; for K = 2048, 15 bits, a
+//            step of 3e-5 samples, 8x finer than float32 resolves f near K);
+//            an IQ entry is {row, fraction, cos, sin} in float32;
+//   phase C: each group walks its voxel's list U entries per trip, software
+//            pipelined: the row loads of the next trip are issued before the
+//            FMAs of the current one, so a warp keeps two trips of loads in
+//            flight; the groups of a warp run independently.
 #include "das_device.cuh"
 
 // tuning: receivers per phase-C trip when a lane holds one chunk (J = 1), the
-// CTAs per SM the register allocation must allow, and whether the warps of a
-// CTA meet at a barrier after every block of receivers
+// CTAs per SM the register allocation must allow for real records with J = 1,
+// whether the warps of a CTA meet at a barrier after every block of
+// receivers, and the warps per CTA
 #ifndef DAS_BRICK_U1
 #define DAS_BRICK_U1 2
 #endif
@@ -61,14 +67,25 @@ struct BrickShape {
     static constexpr int BX = V >= 512 ? 32 : (V >= 128 ? 16 : (V >= 32 ? 8 : 4));
 };
 
-// {row as int bits, fraction} or, for IQ, {row, fraction, cos, sin}
+// packed {relative row, fraction} word, or, for IQ, {row, fraction, cos, sin}
 template <bool CPLX>
-using Entry = typename std::conditional<CPLX, float4, float2>::type;
+using Entry = typename std::conditional<CPLX, float4, unsigned>::type;
 
-// entries per voxel list: MC plus padding, chosen so a list starts on a
-// 16-byte boundary and consecutive voxels start 4 banks apart
+// entries per voxel list: MC plus padding, so that a list starts on an 8-byte
+// (IQ: 16-byte) boundary and the lists of a warp's voxels start in different banks
 template <bool CPLX>
 constexpr int entry_stride() { return CPLX ? MC + 1 : MC + 2; }
+
+// fraction bits of a packed entry for records of K samples: the relative row
+// (< 32 (K + 3)) takes the high bits, the fraction the rest (at most 23)
+inline int fraction_bits(int K)
+{
+    const long long span = 32LL * (K + 3);
+    int rel_bits = 0;
+    while ((1LL << rel_bits) < span) ++rel_bits;
+    const int fb = 32 - rel_bits;
+    return fb > 23 ? 23 : fb;
+}
 
 template <int G, bool CPLX>
 size_t smem_bytes(int Q)
@@ -77,19 +94,28 @@ size_t smem_bytes(int Q)
     return sizeof(Entry<CPLX>) * 2 * V * entry_stride<CPLX>() + sizeof(float2) * (size_t)V * Q;
 }
 
+// One pipelined trip of phase C: U entries, their fractions (and phases) and
+// the two rows of each, J 16-byte chunks per row.
+template <int U, int J, bool CPLX>
+struct Trip {
+    float a[U];
+    float2 ph[U];
+    float4 s0[U][J], s1[U][J];
+};
+
 // acc[c][.] += w0 * s0[c] + w1 * s1[c], w1 = wq * fraction, w0 = wq - w1
 // (IQ: both weights rotated by the entry's phase)
-template <int J, bool CPLX, typename T, typename E>
-__device__ __forceinline__ void accumulate(T (&acc)[J][CPLX ? 2 : 4], float wq, const E &e,
+template <int J, bool CPLX, typename T>
+__device__ __forceinline__ void accumulate(T (&acc)[J][CPLX ? 2 : 4], float wq, float a, float2 ph,
                                            const float4 (&s0)[J], const float4 (&s1)[J])
 {
-    const float w1 = wq * e.y;
+    const float w1 = wq * a;
     const float w0 = wq - w1;
 #pragma unroll
     for (int c = 0; c < J; ++c) {
         if constexpr (CPLX) {
-            const float2 W0 = make_float2(w0 * e.z, w0 * e.w);
-            const float2 W1 = make_float2(w1 * e.z, w1 * e.w);
+            const float2 W0 = make_float2(w0 * ph.x, w0 * ph.y);
+            const float2 W1 = make_float2(w1 * ph.x, w1 * ph.y);
             cfma(acc[c][0], W0, make_float2(s0[c].x, s0[c].y));
             cfma(acc[c][1], W0, make_float2(s0[c].z, s0[c].w));
             cfma(acc[c][0], W1, make_float2(s1[c].x, s1[c].y));
@@ -103,11 +129,16 @@ __device__ __forceinline__ void accumulate(T (&acc)[J][CPLX ? 2 : 4], float wq, 
     }
 }
 
+// CTAs per SM the register allocation must allow: lanes that hold more chunks
+// (J) or complex samples keep more row data in flight per trip
+template <int J, bool CPLX>
+constexpr int min_blocks() { return J >= 4 ? 2 : (J == 2 || CPLX ? 3 : DAS_BRICK_MIN_BLOCKS); }
+
 template <int G, int J, bool CPLX>
-__global__ void __launch_bounds__(THREADS, DAS_BRICK_MIN_BLOCKS)
+__global__ void __launch_bounds__(THREADS, min_blocks<J, CPLX>())
 das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__ perm,
                  const float *__restrict__ tau, const float *__restrict__ wtx,
-                 float *__restrict__ out, int bricks_x, int bricks_y)
+                 float *__restrict__ out, int bricks_x, int bricks_y, int fb)
 {
     constexpr int NW = 32 / G;                     // voxels per warp
     constexpr int V = WARPS * NW;                  // voxels per CTA
@@ -152,6 +183,8 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restric
     const int t = lane % G;
     const char *permB = reinterpret_cast<const char *>(perm) + t * 16;
     const unsigned below = (1u << lane) - 1u;
+    const unsigned frac_mask = (1u << fb) - 1u;
+    const float frac_scale = (float)(1u << fb);
 
     T acc[J][CH];
 #pragma unroll
@@ -183,7 +216,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restric
                 E *eb = ent + (q & 1) * NW * ES;
                 // ---- phase B: compacted entry lists of the warp's voxels
                 int n_mine = 0;
-                const int slab = (q * g.M + m) * KP;
+                const int base_row = (q * g.M + m0) * KP;    // row 0 of this block's first slab
 #pragma unroll
                 for (int i = 0; i < NW; ++i) {
                     const float f = tx[(v0 + i) * g.Q + q].x + dist[i];
@@ -193,14 +226,14 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restric
                     const bool ok = (fl >= -1.f) && (fl <= (float)(g.K - 1));
                     const unsigned bal = __ballot_sync(0xffffffffu, ok);
                     if (ok) {
-                        const int row = slab + (int)fl + 1;
-                        const float a = f - fl;
+                        const int rel = lane * KP + (int)fl + 1;  // row within this block
+                        const float a = f - fl;                   // in [0, 1)
                         E e;
                         if constexpr (CPLX) {
                             const float2 ph = demod_phase(g, f);
-                            e = make_float4(__int_as_float(row), a, ph.x, ph.y);
+                            e = make_float4(__int_as_float(base_row + rel), a, ph.x, ph.y);
                         } else {
-                            e = make_float2(__int_as_float(row), a);
+                            e = ((unsigned)rel << fb) | __float2uint_rz(a * frac_scale);
                         }
                         eb[i * ES + __popc(bal & below)] = e;
                     }
@@ -208,47 +241,84 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restric
                 }
                 __syncwarp();
 
-                // ---- phase C: this group's list, U entries per trip
+                // ---- phase C: this group's list, U entries per trip, pipelined
                 const float wq = tx[(v0 + grp) * g.Q + q].y;
                 const E *ev = eb + grp * ES;
-                int i = 0;
-                for (; i + U <= n_mine; i += U) {
+                // entries -> fractions and row loads of one trip starting at list index i
+                auto load_trip = [&](Trip<U, J, CPLX> &tr, int i) {
                     E e[U];
                     if constexpr (!CPLX && U % 2 == 0) {
-                        // two 8-byte entries per 16-byte shared load
 #pragma unroll
                         for (int u = 0; u < U; u += 2) {
-                            const float4 two = *reinterpret_cast<const float4 *>(ev + i + u);
-                            e[u] = make_float2(two.x, two.y);
-                            e[u + 1] = make_float2(two.z, two.w);
+                            const uint2 two = *reinterpret_cast<const uint2 *>(ev + i + u);
+                            e[u] = two.x;
+                            e[u + 1] = two.y;
                         }
                     } else {
 #pragma unroll
                         for (int u = 0; u < U; ++u) e[u] = ev[i + u];
                     }
-                    float4 s0[U][J], s1[U][J];
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
-                        const char *p0 = permB + (long long)__float_as_int(e[u].x) * ROWB;
+                        int row;
+                        if constexpr (CPLX) {
+                            row = __float_as_int(e[u].x);
+                            tr.a[u] = e[u].y;
+                            tr.ph[u] = make_float2(e[u].z, e[u].w);
+                        } else {
+                            row = base_row + (int)(e[u] >> fb);
+                            // fraction bits placed in a float mantissa of [1, 2), minus 1
+                            tr.a[u] = __int_as_float(0x3f800000 | ((e[u] & frac_mask) << (23 - fb))) - 1.f;
+                            tr.ph[u] = make_float2(1.f, 0.f);
+                        }
+                        const char *p0 = permB + (long long)row * ROWB;
 #pragma unroll
                         for (int c = 0; c < J; ++c) {
-                            s0[u][c] = __ldg(reinterpret_cast<const float4 *>(p0 + c * G * 16));
-                            s1[u][c] = __ldg(reinterpret_cast<const float4 *>(p0 + ROWB + c * G * 16));
+                            tr.s0[u][c] = __ldg(reinterpret_cast<const float4 *>(p0 + c * G * 16));
+                            tr.s1[u][c] = __ldg(reinterpret_cast<const float4 *>(p0 + ROWB + c * G * 16));
                         }
                     }
+                };
+                auto use_trip = [&](const Trip<U, J, CPLX> &tr) {
 #pragma unroll
-                    for (int u = 0; u < U; ++u) accumulate<J, CPLX>(acc, wq, e[u], s0[u], s1[u]);
+                    for (int u = 0; u < U; ++u) accumulate<J, CPLX>(acc, wq, tr.a[u], tr.ph[u], tr.s0[u], tr.s1[u]);
+                };
+                int i = 0;
+                if (n_mine >= U) {
+                    Trip<U, J, CPLX> ta, tb;
+                    load_trip(ta, 0);
+                    i = U;
+                    for (;;) {
+                        if (i + U > n_mine) { use_trip(ta); break; }
+                        load_trip(tb, i);
+                        i += U;
+                        use_trip(ta);
+                        if (i + U > n_mine) { use_trip(tb); break; }
+                        load_trip(ta, i);
+                        i += U;
+                        use_trip(tb);
+                    }
                 }
                 for (; i < n_mine; ++i) {
+                    Trip<1, J, CPLX> t1;
                     const E e = ev[i];
-                    float4 s0[J], s1[J];
-                    const char *p0 = permB + (long long)__float_as_int(e.x) * ROWB;
+                    int row;
+                    if constexpr (CPLX) {
+                        row = __float_as_int(e.x);
+                        t1.a[0] = e.y;
+                        t1.ph[0] = make_float2(e.z, e.w);
+                    } else {
+                        row = base_row + (int)(e >> fb);
+                        t1.a[0] = __int_as_float(0x3f800000 | ((e & frac_mask) << (23 - fb))) - 1.f;
+                        t1.ph[0] = make_float2(1.f, 0.f);
+                    }
+                    const char *p0 = permB + (long long)row * ROWB;
 #pragma unroll
                     for (int c = 0; c < J; ++c) {
-                        s0[c] = __ldg(reinterpret_cast<const float4 *>(p0 + c * G * 16));
-                        s1[c] = __ldg(reinterpret_cast<const float4 *>(p0 + ROWB + c * G * 16));
+                        t1.s0[0][c] = __ldg(reinterpret_cast<const float4 *>(p0 + c * G * 16));
+                        t1.s1[0][c] = __ldg(reinterpret_cast<const float4 *>(p0 + ROWB + c * G * 16));
                     }
-                    accumulate<J, CPLX>(acc, wq, e, s0, s1);
+                    accumulate<J, CPLX>(acc, wq, t1.a[0], t1.ph[0], t1.s0[0], t1.s1[0]);
                 }
                 // the next transmit writes the other buffer; the one after that
                 // comes after the next __syncwarp
@@ -286,7 +356,8 @@ cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, cons
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     das_brick_kernel<G, J, CPLX><<<(int)blocks, THREADS, smem, stream>>>(
-        g, rx, static_cast<const float *>(perm), tau, w, static_cast<float *>(out), bricks_x, bricks_y);
+        g, rx, static_cast<const float *>(perm), tau, w, static_cast<float *>(out), bricks_x, bricks_y,
+        fraction_bits(g.K));
     return cudaGetLastError();
 }
 
@@ -310,7 +381,7 @@ bool choose(int B, bool cplx, int &G, int &J)
 bool brick_supported(int B, bool cplx, int K)
 {
     int G, J;
-    return K >= 2 && choose(B, cplx, G, J);
+    return K >= 2 && fraction_bits(K) >= 10 && choose(B, cplx, G, J);
 }
 
 cudaError_t launch_brick(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
