@@ -332,7 +332,8 @@ def run_ours(args, world, rank, local):
                "h2d_bytes_per_step": int(rf_h.numel() * rf_h.element_size() + 2 * tau_h.numel() * 4),
                "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size()),
                "ms_per_step": 1e3 * e2e_s}
-        if not torch.equal(out_h, out.cpu()):
+        ref = out.cpu()
+        if float((out_h - ref).abs().max()) > 1e-5 * float(ref.abs().max()):
             raise RuntimeError("host entry point disagrees with the device entry point")
 
     # ---------------- roofline of the dominant kernel (the DAS kernel)

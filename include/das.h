@@ -83,7 +83,12 @@ typedef enum {
     DAS_OPT_TIMING = 2,    /* 1: record CUDA events around the permute and the DAS
                               kernel of each das_beamform (read them with
                               das_plan_last_times); 0 (default): no events */
-    DAS_OPT_BI_GROUP = 3   /* BI kernel: lanes per voxel G in {2,4,8,16,32}; 0 = automatic */
+    DAS_OPT_BI_GROUP = 3,  /* BI kernel: lanes per voxel G in {2,4,8,16,32}; 0 = automatic */
+    DAS_OPT_HOST_GROUPS = 4 /* das_beamform_host with the brick kernel: number of transmit
+                              groups the record is streamed in (copy of group g+1
+                              overlapping the permute and sum of group g); 0 (default) =
+                              min(Q, 5), 1 = copy everything first.  Summing in groups
+                              changes the float32 rounding order, not the result beyond it */
 } das_option;
 
 /* Regular voxel grid: voxel n = ix + nx*(iy + ny*iz) sits at
@@ -143,9 +148,13 @@ das_status das_beamform(das_plan plan, const void *rf, const float *tau_tx,
 
 /*
  * The same computation from host buffers (same layouts as das_beamform, host
- * memory): copies the inputs to plan-owned device buffers on `stream`, runs
- * das_beamform, copies y back and synchronises the stream before returning.
- * Device buffers (about the size of rf) are allocated on first use and kept.
+ * memory): copies the inputs to plan-owned device buffers, computes, copies y
+ * back and synchronises `stream` before returning.  With the brick kernel the
+ * record is streamed in groups of transmits (DAS_OPT_HOST_GROUPS) on an internal
+ * copy stream, so the copy of one group overlaps the permute and sum of the
+ * previous one; the other kernels copy everything, then run das_beamform.
+ * Device buffers (about the size of rf) and the copy stream are created on first
+ * use and kept.  Page-locked host memory is needed for the overlap.
  * Errors: as das_beamform.  Synchronous.
  */
 das_status das_beamform_host(das_plan plan, const void *rf_host, const float *tau_tx_host,

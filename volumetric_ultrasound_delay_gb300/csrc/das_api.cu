@@ -55,9 +55,12 @@ struct das_plan_s {
     void *d_perm = nullptr;
     size_t perm_bytes = 0;
     bool perm_pads_zero = false;   // scratch holds the padded layout with zero pad rows
-    // device staging of das_beamform_host
+    // device staging of das_beamform_host, and its copy stream / events
     void *d_rf = nullptr, *d_out = nullptr;
     float *d_tau = nullptr, *d_w = nullptr;
+    int host_groups = 0;                      // DAS_OPT_HOST_GROUPS (0 = automatic)
+    cudaStream_t copy_stream = nullptr;
+    std::vector<cudaEvent_t> copy_ev;         // [0]: start, [1]: tau/w copied, [2+g]: group g copied
     DasGeom geom{};
 
     size_t elem_bytes() const { return dtype == DAS_C64 ? 8 : 4; }
@@ -109,6 +112,33 @@ void release(das_plan_s *p)
     cudaFree(p->d_w);
     for (auto &e : p->ev)
         if (e) cudaEventDestroy(e);
+    for (auto &e : p->copy_ev)
+        if (e) cudaEventDestroy(e);
+    if (p->copy_stream) cudaStreamDestroy(p->copy_stream);
+}
+
+// Allocates the permute scratch on first use (sized for the padded layout, the
+// larger one) and zeroes it when the padded layout is about to be used after
+// the scratch held something else; the permute never writes the pad rows.
+das_status ensure_scratch(das_plan_s *p, int layout, cudaStream_t stream)
+{
+    if (!p->d_perm) {
+        cudaError_t e = cudaMalloc(&p->d_perm, p->padded_bytes());
+        if (e != cudaSuccess) {
+            p->d_perm = nullptr;
+            cudaGetLastError();
+            return cuda_fail(e, "permute scratch allocation");
+        }
+        p->perm_bytes = p->padded_bytes();
+        p->perm_pads_zero = false;
+    }
+    if (layout == 2 && !p->perm_pads_zero) {
+        cudaError_t e = cudaMemsetAsync(p->d_perm, 0, p->padded_bytes(), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "zeroing the permute scratch");
+        p->perm_pads_zero = true;
+    }
+    if (layout == 0) p->perm_pads_zero = false;
+    return DAS_OK;
 }
 
 // Restores the caller's current device on scope exit.
@@ -234,6 +264,13 @@ das_status das_plan_set_option(das_plan p, int option, double value)
         p->timing = (int)value;
         p->timed_once = false;
         return DAS_OK;
+    case DAS_OPT_HOST_GROUPS: {
+        const int n = (int)value;
+        if ((double)n != value || n < 0 || n > 64)
+            return fail(DAS_ERR_INVALID_ARG, "host groups must be an integer in [0, 64]");
+        p->host_groups = n;
+        return DAS_OK;
+    }
     case DAS_OPT_BI_GROUP: {
         const int gsz = (int)value;
         if ((double)gsz != value || !(gsz == 0 || gsz == 2 || gsz == 4 || gsz == 8 || gsz == 16 || gsz == 32))
@@ -253,6 +290,7 @@ das_status das_plan_get_option(das_plan p, int option, double *value)
     case DAS_OPT_DEMOD_HZ: *value = p->f_demod; return DAS_OK;
     case DAS_OPT_TIMING: *value = p->timing; return DAS_OK;
     case DAS_OPT_BI_GROUP: *value = p->bi_group; return DAS_OK;
+    case DAS_OPT_HOST_GROUPS: *value = p->host_groups; return DAS_OK;
     default: return fail(DAS_ERR_INVALID_ARG, "unknown option %d", option);
     }
 }
@@ -282,24 +320,10 @@ das_status das_beamform(das_plan p, const void *rf, const float *tau_tx, const f
     const void *src = rf;
     const bool permute = kernel != DAS_KERNEL_BL;
     const int layout = kernel == DAS_KERNEL_BI ? 0 : 2;
-    if (permute && !p->d_perm) {
-        // sized for the padded layout, which is the larger of the two
-        cudaError_t e = cudaMalloc(&p->d_perm, p->padded_bytes());
-        if (e != cudaSuccess) {
-            p->d_perm = nullptr;
-            cudaGetLastError();
-            return cuda_fail(e, "permute scratch allocation");
-        }
-        p->perm_bytes = p->padded_bytes();
-        p->perm_pads_zero = false;
+    if (permute) {
+        das_status st2 = ensure_scratch(p, layout, stream);
+        if (st2 != DAS_OK) return st2;
     }
-    if (permute && layout == 2 && !p->perm_pads_zero) {
-        // the pad rows are never written by the permute, so zeroing once suffices
-        cudaError_t e = cudaMemsetAsync(p->d_perm, 0, p->padded_bytes(), stream);
-        if (e != cudaSuccess) return cuda_fail(e, "zeroing the permute scratch");
-        p->perm_pads_zero = true;
-    }
-    if (permute && layout == 0) p->perm_pads_zero = false;
     cudaError_t e = cudaSuccess;
     if (p->timing) e = cudaEventRecord(p->ev[0], stream);
     if (e == cudaSuccess && permute) {
@@ -331,6 +355,9 @@ das_status das_beamform_host(das_plan p, const void *rf_host, const float *tau_t
 {
     if (!p) return fail(DAS_ERR_INVALID_ARG, "plan is NULL");
     if (!rf_host || !tau_tx_host || !w_tx_host || !out_host) return fail(DAS_ERR_INVALID_ARG, "NULL buffer");
+    const int kernel = resolve_kernel(p);
+    das_status st = check_supported(p, kernel);
+    if (st != DAS_OK) return st;
     DeviceGuard dg(p->device);
     cudaError_t e = cudaSuccess;
     if (!p->d_rf) e = cudaMalloc(&p->d_rf, p->rf_bytes());
@@ -341,12 +368,63 @@ das_status das_beamform_host(das_plan p, const void *rf_host, const float *tau_t
         cudaGetLastError();
         return cuda_fail(e, "host-path device buffers");
     }
-    e = cudaMemcpyAsync(p->d_rf, rf_host, p->rf_bytes(), cudaMemcpyHostToDevice, stream);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(p->d_tau, tau_tx_host, p->txw_bytes(), cudaMemcpyHostToDevice, stream);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(p->d_w, w_tx_host, p->txw_bytes(), cudaMemcpyHostToDevice, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
-    das_status st = das_beamform(p, p->d_rf, p->d_tau, p->d_w, p->d_out, stream);
-    if (st != DAS_OK) return st;
+    int groups = p->host_groups > 0 ? p->host_groups : (p->Q < 5 ? p->Q : 5);
+    if (kernel != DAS_KERNEL_BRICK) groups = 1;     // only the brick kernel sums transmit ranges
+    if (groups > p->Q) groups = p->Q;
+
+    if (groups <= 1) {
+        e = cudaMemcpyAsync(p->d_rf, rf_host, p->rf_bytes(), cudaMemcpyHostToDevice, stream);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(p->d_tau, tau_tx_host, p->txw_bytes(), cudaMemcpyHostToDevice, stream);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(p->d_w, w_tx_host, p->txw_bytes(), cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+        st = das_beamform(p, p->d_rf, p->d_tau, p->d_w, p->d_out, stream);
+        if (st != DAS_OK) return st;
+    } else {
+        // Streamed: the record arrives in groups of transmits on a copy stream
+        // while `stream` permutes and sums the groups already on the device.
+        if (!p->copy_stream) {
+            e = cudaStreamCreateWithFlags(&p->copy_stream, cudaStreamNonBlocking);
+            if (e != cudaSuccess) { p->copy_stream = nullptr; return cuda_fail(e, "copy stream"); }
+        }
+        while ((int)p->copy_ev.size() < groups + 2) {
+            cudaEvent_t ev;
+            e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+            if (e != cudaSuccess) return cuda_fail(e, "copy events");
+            p->copy_ev.push_back(ev);
+        }
+        const bool cplx = p->dtype == DAS_C64;
+        const size_t eb = p->elem_bytes();
+        const size_t plane = (size_t)p->M * p->K * eb;            // one transmit of one frame
+        const size_t pitch = (size_t)p->Q * plane;                // one frame
+        // nothing queued earlier on `stream` may still read the staging buffers
+        e = cudaEventRecord(p->copy_ev[0], stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(p->copy_stream, p->copy_ev[0], 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(p->d_tau, tau_tx_host, p->txw_bytes(), cudaMemcpyHostToDevice, p->copy_stream);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(p->d_w, w_tx_host, p->txw_bytes(), cudaMemcpyHostToDevice, p->copy_stream);
+        if (e == cudaSuccess) e = cudaEventRecord(p->copy_ev[1], p->copy_stream);
+        for (int gi = 0; gi < groups && e == cudaSuccess; ++gi) {
+            const int q0 = gi * p->Q / groups, q1 = (gi + 1) * p->Q / groups;
+            e = cudaMemcpy2DAsync(static_cast<char *>(p->d_rf) + q0 * plane, pitch,
+                                  static_cast<const char *>(rf_host) + q0 * plane, pitch,
+                                  (q1 - q0) * plane, p->B, cudaMemcpyHostToDevice, p->copy_stream);
+            if (e == cudaSuccess) e = cudaEventRecord(p->copy_ev[2 + gi], p->copy_stream);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+        st = ensure_scratch(p, 2, stream);
+        if (st != DAS_OK) return st;
+        e = cudaStreamWaitEvent(stream, p->copy_ev[1], 0);
+        for (int gi = 0; gi < groups && e == cudaSuccess; ++gi) {
+            const int q0 = gi * p->Q / groups, q1 = (gi + 1) * p->Q / groups;
+            e = cudaStreamWaitEvent(stream, p->copy_ev[2 + gi], 0);
+            if (e == cudaSuccess)
+                e = das::launch_permute(p->d_rf, p->d_perm, (int)eb, p->B, p->Q, p->M, p->K, 2,
+                                        p->num_sms, stream, q0, q1);
+            if (e == cudaSuccess)
+                e = das::launch_brick(p->geom, p->d_rx, p->d_perm, p->d_tau, p->d_w, p->d_out, cplx,
+                                      stream, q0, q1, gi > 0);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "streamed beamform launch");
+    }
     e = cudaMemcpyAsync(out_host, p->d_out, p->out_bytes(), cudaMemcpyDeviceToHost, stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");

@@ -138,7 +138,8 @@ template <int G, int J, bool CPLX>
 __global__ void __launch_bounds__(THREADS, min_blocks<J, CPLX>())
 das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__ perm,
                  const float *__restrict__ tau, const float *__restrict__ wtx,
-                 float *__restrict__ out, int bricks_x, int bricks_y, int fb)
+                 float *__restrict__ out, int bricks_x, int bricks_y, int fb, int q_begin,
+                 int q_end, int add_to_out)
 {
     constexpr int NW = 32 / G;                     // voxels per warp
     constexpr int V = WARPS * NW;                  // voxels per CTA
@@ -212,7 +213,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restric
             }
         }
         if (__ballot_sync(0xffffffffu, any) != 0u) {
-            for (int q = 0; q < g.Q; ++q) {
+            for (int q = q_begin; q < q_end; ++q) {
                 E *eb = ent + (q & 1) * NW * ES;
                 // ---- phase B: compacted entry lists of the warp's voxels
                 int n_mine = 0;
@@ -337,12 +338,21 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restric
 #pragma unroll
     for (int c = 0; c < J; ++c)
 #pragma unroll
-        for (int e = 0; e < CH; ++e) outT[(long long)((t + c * G) * CH + e) * g.N + n] = acc[c][e];
+        for (int e = 0; e < CH; ++e) {
+            T *o = outT + (long long)((t + c * G) * CH + e) * g.N + n;
+            if (add_to_out) {
+                T prev = *o;
+                if constexpr (CPLX) *o = make_float2(prev.x + acc[c][e].x, prev.y + acc[c][e].y);
+                else *o = prev + acc[c][e];
+            } else {
+                *o = acc[c][e];
+            }
+        }
 }
 
 template <int G, int J, bool CPLX>
 cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
-                       const float *w, void *out, cudaStream_t stream)
+                       const float *w, void *out, cudaStream_t stream, int q0, int q1, bool acc)
 {
     constexpr int V = WARPS * (32 / G);
     constexpr int BX = BrickShape<V>::BX;
@@ -357,7 +367,7 @@ cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, cons
     if (err != cudaSuccess) return err;
     das_brick_kernel<G, J, CPLX><<<(int)blocks, THREADS, smem, stream>>>(
         g, rx, static_cast<const float *>(perm), tau, w, static_cast<float *>(out), bricks_x, bricks_y,
-        fraction_bits(g.K));
+        fraction_bits(g.K), q0, q1, acc ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -385,14 +395,17 @@ bool brick_supported(int B, bool cplx, int K)
 }
 
 cudaError_t launch_brick(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
-                         const float *w, void *out, bool cplx, cudaStream_t stream)
+                         const float *w, void *out, bool cplx, cudaStream_t stream, int q0, int q1,
+                         bool accumulate)
 {
     int G, J;
+    if (q1 < 0) q1 = g.Q;
+    if (q0 < 0 || q0 > q1 || q1 > g.Q) return cudaErrorInvalidValue;
     if (g.K < 2 || !choose(g.B, cplx, G, J)) return cudaErrorInvalidValue;
 #define DAS_BRICK_CASE(GG, JJ)                                                                  \
     if (G == GG && J == JJ)                                                                     \
-        return cplx ? launch_one<GG, JJ, true>(g, rx, perm, tau, w, out, stream)                \
-                    : launch_one<GG, JJ, false>(g, rx, perm, tau, w, out, stream);
+        return cplx ? launch_one<GG, JJ, true>(g, rx, perm, tau, w, out, stream, q0, q1, accumulate) \
+                    : launch_one<GG, JJ, false>(g, rx, perm, tau, w, out, stream, q0, q1, accumulate);
     DAS_BRICK_CASE(2, 1) DAS_BRICK_CASE(4, 1) DAS_BRICK_CASE(8, 1)
     DAS_BRICK_CASE(8, 2) DAS_BRICK_CASE(8, 4)
 #undef DAS_BRICK_CASE

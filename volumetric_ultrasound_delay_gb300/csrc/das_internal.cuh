@@ -32,15 +32,19 @@ namespace das {
 void record_error(const char *msg);
 
 // Launchers (each returns the cudaError_t of its launch).
+// Permutes the planes of transmits [q0, q1) (q1 < 0: all Q).
 cudaError_t launch_permute(const void *in, void *out, int elem_bytes, int B, int Q, int M, int K,
-                           int layout, int num_sms, cudaStream_t stream);
+                           int layout, int num_sms, cudaStream_t stream, int q0 = 0, int q1 = -1);
 cudaError_t launch_bl(const DasGeom &g, const RxPos *rx, const void *rf, const float *tau,
                       const float *w, void *out, bool cplx, cudaStream_t stream);
 bool bi_supported(int B, bool cplx, int group);
 cudaError_t launch_bi(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
                       const float *w, void *out, bool cplx, int group, cudaStream_t stream);
 bool brick_supported(int B, bool cplx, int K);
+// Sums transmits [q0, q1) (q1 < 0: all Q); with accumulate, adds to out
+// instead of overwriting it.
 cudaError_t launch_brick(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
-                         const float *w, void *out, bool cplx, cudaStream_t stream);
+                         const float *w, void *out, bool cplx, cudaStream_t stream, int q0 = 0,
+                         int q1 = -1, bool accumulate = false);
 
 }  // namespace das

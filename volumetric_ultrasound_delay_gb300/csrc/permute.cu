@@ -30,7 +30,7 @@ template <typename T>
 __global__ void __launch_bounds__(THREADS)
 permute_kernel(const T *__restrict__ in, T *__restrict__ out, int B, int QM, int K,
                long long osk, long long osqm, long long n_blocks, int blocks_b, int blocks_k,
-               int vec_in, int vec_out)
+               int vec_in, int vec_out, int qm0)
 {
     constexpr int V = 16 / sizeof(T);            // elements per 16-byte vector
     constexpr int VPR = TILE / V;                // vectors per 32-element row
@@ -41,7 +41,7 @@ permute_kernel(const T *__restrict__ in, T *__restrict__ out, int B, int QM, int
         const int tk = (int)(t % blocks_k);
         const long long r = t / blocks_k;
         const int tb = (int)(r % blocks_b);
-        const int qm = (int)(r / blocks_b);
+        const int qm = qm0 + (int)(r / blocks_b);
         const int b0 = tb * TILE;
         const int k0 = tk * TILE * SUB;
 
@@ -104,7 +104,7 @@ permute_kernel(const T *__restrict__ in, T *__restrict__ out, int B, int QM, int
 
 template <typename T>
 cudaError_t launch_typed(const void *in, void *out, int B, int Q, int M, int K, int layout,
-                         int num_sms, cudaStream_t stream)
+                         int num_sms, cudaStream_t stream, int q0, int q1)
 {
     constexpr int V = 16 / sizeof(T);
     const int QM = Q * M;
@@ -114,7 +114,7 @@ cudaError_t launch_typed(const void *in, void *out, int B, int Q, int M, int K, 
     if (layout == 2) out = static_cast<T *>(out) + B;   // row k = 0 of slab 0
     const int blocks_b = (B + TILE - 1) / TILE;
     const int blocks_k = (K + TILE * SUB - 1) / (TILE * SUB);
-    const long long n_blocks = (long long)QM * blocks_b * blocks_k;
+    const long long n_blocks = (long long)(q1 - q0) * M * blocks_b * blocks_k;
     if (n_blocks == 0) return cudaSuccess;
     const bool in_al = (reinterpret_cast<uintptr_t>(in) % 16) == 0;
     const bool out_al = (reinterpret_cast<uintptr_t>(out) % 16) == 0;
@@ -124,19 +124,21 @@ cudaError_t launch_typed(const void *in, void *out, int B, int Q, int M, int K, 
     const int grid = (int)(n_blocks < cap ? n_blocks : cap);
     permute_kernel<T><<<grid, THREADS, 0, stream>>>(
         static_cast<const T *>(in), static_cast<T *>(out), B, QM, K, osk, osqm, n_blocks,
-        blocks_b, blocks_k, vec_in, vec_out);
+        blocks_b, blocks_k, vec_in, vec_out, q0 * M);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_permute(const void *in, void *out, int elem_bytes, int B, int Q, int M, int K,
-                           int layout, int num_sms, cudaStream_t stream)
+                           int layout, int num_sms, cudaStream_t stream, int q0, int q1)
 {
+    if (q1 < 0) q1 = Q;
+    if (q0 < 0 || q0 > q1 || q1 > Q) return cudaErrorInvalidValue;
     switch (elem_bytes) {
-    case 2: return launch_typed<unsigned short>(in, out, B, Q, M, K, layout, num_sms, stream);
-    case 4: return launch_typed<float>(in, out, B, Q, M, K, layout, num_sms, stream);
-    case 8: return launch_typed<float2>(in, out, B, Q, M, K, layout, num_sms, stream);
+    case 2: return launch_typed<unsigned short>(in, out, B, Q, M, K, layout, num_sms, stream, q0, q1);
+    case 4: return launch_typed<float>(in, out, B, Q, M, K, layout, num_sms, stream, q0, q1);
+    case 8: return launch_typed<float2>(in, out, B, Q, M, K, layout, num_sms, stream, q0, q1);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -23,7 +23,7 @@ DAS_OK, DAS_ERR_INVALID_ARG, DAS_ERR_UNSUPPORTED, DAS_ERR_OUT_OF_MEMORY, DAS_ERR
 DAS_F32, DAS_C64 = 0, 1
 KERNELS = {"auto": 0, "bl": 1, "bi": 2, "brick": 3}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
-OPT_KERNEL, OPT_DEMOD_HZ, OPT_TIMING, OPT_BI_GROUP = 0, 1, 2, 3
+OPT_KERNEL, OPT_DEMOD_HZ, OPT_TIMING, OPT_BI_GROUP, OPT_HOST_GROUPS = 0, 1, 2, 3, 4
 
 # every function the header declares, with its ctypes signature
 _VP = ctypes.c_void_p
