@@ -84,12 +84,26 @@ typedef enum {
                               kernel of each das_beamform (read them with
                               das_plan_last_times); 0 (default): no events */
     DAS_OPT_BI_GROUP = 3,  /* BI kernel: lanes per voxel G in {2,4,8,16,32}; 0 = automatic */
+    DAS_OPT_STORAGE = 5,   /* das_storage value: element type of the permuted copy */
     DAS_OPT_HOST_GROUPS = 4 /* das_beamform_host with the brick kernel: number of transmit
                               groups the record is streamed in (copy of group g+1
                               overlapping the permute and sum of group g); 0 (default) =
                               min(Q, 5), 1 = copy everything first.  Summing in groups
                               changes the float32 rounding order, not the result beyond it */
 } das_option;
+
+/* Element type of the permuted copy of the record (DAS_OPT_STORAGE).
+ * DAS_STORAGE_F16 rounds each float32 sample (complex64: each component) to
+ * half precision in the permute and converts back to float32 before the
+ * interpolation and the sum (ffdas paper, Methods, FP16 paragraphs; ffdas docs,
+ * "Mixed-precision storage"): it halves the bytes the kernel reads, and y is
+ * then DAS of the half-rounded record.  Served by the brick kernel only
+ * (B * 2 bytes, complex B * 4, a multiple of 16); the other kernels return
+ * DAS_ERR_UNSUPPORTED. */
+typedef enum {
+    DAS_STORAGE_NATIVE = 0,
+    DAS_STORAGE_F16 = 1
+} das_storage;
 
 /* Regular voxel grid: voxel n = ix + nx*(iy + ny*iz) sits at
  * (x0 + ix*dx, y0 + iy*dy, z0 + iz*dz), metres.  The receivers face +z. */
@@ -175,7 +189,9 @@ das_status das_plan_destroy(das_plan plan);
 
 /*
  * RF layout permute (ffdas paper, Methods, batch-inner paragraph: B x Q x M x K
- * with k contiguous -> a layout with b contiguous).  A bit-exact copy.
+ * with k contiguous -> a layout with b contiguous).  A bit-exact copy, or with
+ * storage DAS_STORAGE_F16 a copy rounded to half precision (round to nearest
+ * even; complex: both components), as the half-storage kernels read it.
  *   layout 0: K x Q x M x B (the pages' batch-inner layout, used by BI)
  *   layout 1: Q x M x K x B (rows of one (q, m) adjacent)
  *   layout 2: Q x M x (K+3) x B, sample k of slab (q, m) at row k + 1; rows 0,
@@ -183,11 +199,12 @@ das_status das_plan_destroy(das_plan plan);
  *             keeps them zero, so reads just outside the record return 0)
  *   in       device buffer of B*Q*M*K elements of dtype;
  *   out      device buffer of B*Q*M*K (layouts 0, 1) or B*Q*M*(K+3) (layout 2)
- *            elements; in and out must not overlap.
+ *            elements of dtype, or of half / half2 with DAS_STORAGE_F16; in and
+ *            out must not overlap.
  * Errors: DAS_ERR_INVALID_ARG, DAS_ERR_CUDA.  Asynchronous.
  */
 das_status das_permute(const void *in, void *out, das_dtype dtype, int B, int Q, int M,
-                       int K, int layout, cudaStream_t stream);
+                       int K, int layout, das_storage storage, cudaStream_t stream);
 
 /*
  * das_beamform_noalloc -- the same computation as a plan running the brick

@@ -60,8 +60,9 @@ def test_host_side_rejections(libdas):
     assert libdas.das_plan_set_option(None, 0, 0.0) == das.DAS_ERR_INVALID_ARG
     assert libdas.das_plan_destroy(None) == das.DAS_OK
     # permute argument checks
-    assert libdas.das_permute(None, None, 0, 1, 1, 1, 1, 0, None) == das.DAS_ERR_INVALID_ARG
+    assert libdas.das_permute(None, None, 0, 1, 1, 1, 1, 0, 0, None) == das.DAS_ERR_INVALID_ARG
     buf = ctypes.create_string_buffer(64)
-    assert libdas.das_permute(buf, buf, 0, 1, 1, 1, 4, 0, None) == das.DAS_ERR_INVALID_ARG  # overlap
-    assert libdas.das_permute(buf, ctypes.byref(buf, 32), 0, 1, 1, 1, 4, 3, None) == das.DAS_ERR_INVALID_ARG  # bad layout
+    assert libdas.das_permute(buf, buf, 0, 1, 1, 1, 4, 0, 0, None) == das.DAS_ERR_INVALID_ARG  # overlap
+    assert libdas.das_permute(buf, ctypes.byref(buf, 32), 0, 1, 1, 1, 4, 3, 0, None) == das.DAS_ERR_INVALID_ARG  # bad layout
+    assert libdas.das_permute(buf, ctypes.byref(buf, 32), 0, 1, 1, 1, 4, 0, 7, None) == das.DAS_ERR_INVALID_ARG  # bad storage
     assert libdas.das_version() == b"1.0.0"

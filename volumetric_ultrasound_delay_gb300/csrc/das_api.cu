@@ -59,6 +59,7 @@ struct das_plan_s {
     void *d_rf = nullptr, *d_out = nullptr;
     float *d_tau = nullptr, *d_w = nullptr;
     int host_groups = 0;                      // DAS_OPT_HOST_GROUPS (0 = automatic)
+    int storage = DAS_STORAGE_NATIVE;         // DAS_OPT_STORAGE
     cudaStream_t copy_stream = nullptr;
     std::vector<cudaEvent_t> copy_ev;         // [0]: start, [1]: tau/w copied, [2+g]: group g copied
     DasGeom geom{};
@@ -76,6 +77,7 @@ int resolve_kernel(const das_plan_s *p)
 {
     const bool cplx = p->dtype == DAS_C64;
     if (p->kernel != DAS_KERNEL_AUTO) return p->kernel;
+    if (p->storage == DAS_STORAGE_F16) return DAS_KERNEL_BRICK;   // the only half-storage kernel
     if (das::brick_supported(p->B, cplx, p->K)) return DAS_KERNEL_BRICK;
     if (p->K >= 2 && das::bi_supported(p->B, cplx, p->bi_group)) return DAS_KERNEL_BI;
     return DAS_KERNEL_BL;
@@ -84,6 +86,8 @@ int resolve_kernel(const das_plan_s *p)
 das_status check_supported(const das_plan_s *p, int kernel)
 {
     const bool cplx = p->dtype == DAS_C64;
+    if (p->storage == DAS_STORAGE_F16 && kernel != DAS_KERNEL_BRICK)
+        return fail(DAS_ERR_UNSUPPORTED, "half-precision storage is served by the brick kernel only");
     switch (kernel) {
     case DAS_KERNEL_BL: return DAS_OK;
     case DAS_KERNEL_BI:
@@ -93,10 +97,10 @@ das_status check_supported(const das_plan_s *p, int kernel)
                         "(B=%d, group=%d)", p->B, p->bi_group);
         return DAS_OK;
     case DAS_KERNEL_BRICK:
-        if (!das::brick_supported(p->B, cplx, p->K))
+        if (!das::brick_supported(p->B, cplx, p->K, p->storage == DAS_STORAGE_F16))
             return fail(DAS_ERR_UNSUPPORTED,
-                        "brick kernel needs K >= 2 and B*element size in {32, 64, 128, 256, 512} "
-                        "bytes (B=%d)", p->B);
+                        "brick kernel needs K >= 2 and B * element size in {32, 64, 128, 256, 512} "
+                        "bytes (half storage: {16, ..., 64, 128, 256}) (B=%d)", p->B);
         return DAS_OK;
     default: return fail(DAS_ERR_INVALID_ARG, "unknown kernel %d", kernel);
     }
@@ -264,6 +268,14 @@ das_status das_plan_set_option(das_plan p, int option, double value)
         p->timing = (int)value;
         p->timed_once = false;
         return DAS_OK;
+    case DAS_OPT_STORAGE: {
+        const int v = (int)value;
+        if ((double)v != value || (v != DAS_STORAGE_NATIVE && v != DAS_STORAGE_F16))
+            return fail(DAS_ERR_INVALID_ARG, "storage must be DAS_STORAGE_NATIVE or DAS_STORAGE_F16");
+        if (v != p->storage) p->perm_pads_zero = false;   // pad rows move with the element size
+        p->storage = v;
+        return DAS_OK;
+    }
     case DAS_OPT_HOST_GROUPS: {
         const int n = (int)value;
         if ((double)n != value || n < 0 || n > 64)
@@ -291,6 +303,7 @@ das_status das_plan_get_option(das_plan p, int option, double *value)
     case DAS_OPT_TIMING: *value = p->timing; return DAS_OK;
     case DAS_OPT_BI_GROUP: *value = p->bi_group; return DAS_OK;
     case DAS_OPT_HOST_GROUPS: *value = p->host_groups; return DAS_OK;
+    case DAS_OPT_STORAGE: *value = p->storage; return DAS_OK;
     default: return fail(DAS_ERR_INVALID_ARG, "unknown option %d", option);
     }
 }
@@ -326,9 +339,10 @@ das_status das_beamform(das_plan p, const void *rf, const float *tau_tx, const f
     }
     cudaError_t e = cudaSuccess;
     if (p->timing) e = cudaEventRecord(p->ev[0], stream);
+    const bool half = p->storage == DAS_STORAGE_F16;
     if (e == cudaSuccess && permute) {
         e = das::launch_permute(rf, p->d_perm, (int)p->elem_bytes(), p->B, p->Q, p->M, p->K,
-                                layout, p->num_sms, stream);
+                                layout, p->num_sms, stream, 0, -1, half);
         src = p->d_perm;
     }
     if (e == cudaSuccess && p->timing) e = cudaEventRecord(p->ev[1], stream);
@@ -338,7 +352,9 @@ das_status das_beamform(das_plan p, const void *rf, const float *tau_tx, const f
     case DAS_KERNEL_BI:
         e = das::launch_bi(p->geom, p->d_rx, src, tau_tx, w_tx, out, cplx, p->bi_group, stream);
         break;
-    default: e = das::launch_brick(p->geom, p->d_rx, src, tau_tx, w_tx, out, cplx, stream); break;
+    default:
+        e = das::launch_brick(p->geom, p->d_rx, src, tau_tx, w_tx, out, cplx, stream, 0, -1, false, half);
+        break;
     }
     if (e != cudaSuccess) return cuda_fail(e, "DAS kernel launch");
     if (p->timing) {
@@ -416,12 +432,13 @@ das_status das_beamform_host(das_plan p, const void *rf_host, const float *tau_t
         for (int gi = 0; gi < groups && e == cudaSuccess; ++gi) {
             const int q0 = gi * p->Q / groups, q1 = (gi + 1) * p->Q / groups;
             e = cudaStreamWaitEvent(stream, p->copy_ev[2 + gi], 0);
+            const bool half = p->storage == DAS_STORAGE_F16;
             if (e == cudaSuccess)
                 e = das::launch_permute(p->d_rf, p->d_perm, (int)eb, p->B, p->Q, p->M, p->K, 2,
-                                        p->num_sms, stream, q0, q1);
+                                        p->num_sms, stream, q0, q1, half);
             if (e == cudaSuccess)
                 e = das::launch_brick(p->geom, p->d_rx, p->d_perm, p->d_tau, p->d_w, p->d_out, cplx,
-                                      stream, q0, q1, gi > 0);
+                                      stream, q0, q1, gi > 0, half);
         }
         if (e != cudaSuccess) return cuda_fail(e, "streamed beamform launch");
     }
@@ -469,23 +486,27 @@ das_status das_plan_destroy(das_plan p)
 }
 
 das_status das_permute(const void *in, void *out, das_dtype dtype, int B, int Q, int M, int K,
-                       int layout, cudaStream_t stream)
+                       int layout, das_storage storage, cudaStream_t stream)
 {
     if (!in || !out) return fail(DAS_ERR_INVALID_ARG, "NULL buffer");
     if (dtype != DAS_F32 && dtype != DAS_C64) return fail(DAS_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
     if (B < 1 || Q < 1 || M < 1 || K < 1) return fail(DAS_ERR_INVALID_ARG, "B, Q, M, K must be >= 1");
     if ((long long)Q * M >= (1LL << 31)) return fail(DAS_ERR_INVALID_ARG, "Q*M must be < 2^31");
     if (layout < 0 || layout > 2) return fail(DAS_ERR_INVALID_ARG, "layout must be 0, 1 or 2");
+    if (storage != DAS_STORAGE_NATIVE && storage != DAS_STORAGE_F16)
+        return fail(DAS_ERR_INVALID_ARG, "unknown storage %d", (int)storage);
+    const bool half = storage == DAS_STORAGE_F16;
     const size_t eb = dtype == DAS_C64 ? 8 : 4;
     const size_t bytes = (size_t)B * Q * M * K * eb;
-    const size_t obytes = (size_t)B * Q * M * (K + (layout == 2 ? 3 : 0)) * eb;
+    const size_t obytes = (size_t)B * Q * M * (K + (layout == 2 ? 3 : 0)) * (half ? eb / 2 : eb);
     const char *a = static_cast<const char *>(in);
     const char *b = static_cast<const char *>(out);
     if (a < b + obytes && b < a + bytes) return fail(DAS_ERR_INVALID_ARG, "in and out overlap");
     int dev = 0, sms = 1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = das::launch_permute(in, out, (int)eb, B, Q, M, K, layout, sms, stream);
+    if (e == cudaSuccess)
+        e = das::launch_permute(in, out, (int)eb, B, Q, M, K, layout, sms, stream, 0, -1, half);
     if (e != cudaSuccess) return cuda_fail(e, "permute");
     return DAS_OK;
 }

@@ -8,10 +8,18 @@
 //
 // The record is permuted to the zero-padded layout Q x M x (K+3) x B (sample k
 // of slab (q, m) at row k + 1, rows 0, K+1, K+2 zero), so the two rows a voxel
-// reads for a (q, m) are adjacent 16 * G * J-byte runs and a pair that hangs
-// over either end of the record reads a zero row instead of needing special
-// weights.  A group of G lanes owns one voxel; lane t loads the 16-byte chunks
-// t, t + G, ... of both rows (G = 8: one full 128-byte line per row).
+// reads for a (q, m) are adjacent and a pair that hangs over either end of the
+// record reads a zero row instead of needing special weights.  A group of G
+// lanes owns one voxel and reads the voxel's two rows in 16-byte chunks:
+//   pair mode  : lane t loads chunks t, t + G, ... of both rows (float32 data,
+//                and half-precision rows of more than 64 bytes); G = 8 lanes
+//                cover one 128-byte line per row;
+//   split mode : half-precision rows of at most 64 bytes: the 2 * CPR chunks of
+//                the two adjacent rows go one per lane (G = 2 * CPR), so a group
+//                reads one contiguous run; the partial sums of the two rows are
+//                added by one shuffle at the end.
+// Half-precision samples are converted to float32 before the interpolation
+// and the accumulation (ffdas paper, Methods, FP16 paragraphs).
 //
 // A warp owns NW = 32 / G voxels and does all the work for them itself, so
 // after the per-CTA preload of transmit delays no step needs a CTA barrier:
@@ -33,20 +41,18 @@
 //            pipelined: the row loads of the next trip are issued before the
 //            FMAs of the current one, so a warp keeps two trips of loads in
 //            flight; the groups of a warp run independently.
+#include <cuda_fp16.h>
+
 #include "das_device.cuh"
 
 // tuning: receivers per phase-C trip when a lane holds one chunk (J = 1), the
 // CTAs per SM the register allocation must allow for real records with J = 1,
-// whether the warps of a CTA meet at a barrier after every block of
-// receivers, and the warps per CTA
+// and the warps per CTA
 #ifndef DAS_BRICK_U1
 #define DAS_BRICK_U1 2
 #endif
 #ifndef DAS_BRICK_MIN_BLOCKS
 #define DAS_BRICK_MIN_BLOCKS 5
-#endif
-#ifndef DAS_BRICK_CHUNK_BARRIER
-#define DAS_BRICK_CHUNK_BARRIER 0
 #endif
 #ifndef DAS_BRICK_WARPS
 #define DAS_BRICK_WARPS 8
@@ -87,6 +93,20 @@ inline int fraction_bits(int K)
     return fb > 23 ? 23 : fb;
 }
 
+// Storage of the permuted record as seen by one lane of a group.
+//   EPC  elements per 16-byte chunk (float32 4, complex64 2, half 8, half2 4)
+//   ROWB bytes per row (B * element size)
+//   L    16-byte loads per entry and lane
+//   NA   accumulator chunks per lane
+template <int G, int J, bool CPLX, bool HALF, bool SPLIT>
+struct Layout {
+    static constexpr int ESZ = HALF ? (CPLX ? 4 : 2) : (CPLX ? 8 : 4);
+    static constexpr int EPC = 16 / ESZ;
+    static constexpr int ROWB = SPLIT ? 8 * G : 16 * G * J;
+    static constexpr int L = SPLIT ? 1 : 2 * J;
+    static constexpr int NA = SPLIT ? 1 : J;
+};
+
 template <int G, bool CPLX>
 size_t smem_bytes(int Q)
 {
@@ -95,36 +115,73 @@ size_t smem_bytes(int Q)
 }
 
 // One pipelined trip of phase C: U entries, their fractions (and phases) and
-// the two rows of each, J 16-byte chunks per row.
-template <int U, int J, bool CPLX>
+// the L chunks of each.
+template <int U, int L>
 struct Trip {
     float a[U];
     float2 ph[U];
-    float4 s0[U][J], s1[U][J];
+    uint4 s[U][L];
 };
 
-// acc[c][.] += w0 * s0[c] + w1 * s1[c], w1 = wq * fraction, w0 = wq - w1
-// (IQ: both weights rotated by the entry's phase)
-template <int J, bool CPLX, typename T>
-__device__ __forceinline__ void accumulate(T (&acc)[J][CPLX ? 2 : 4], float wq, float a, float2 ph,
-                                           const float4 (&s0)[J], const float4 (&s1)[J])
+// 16 bytes of samples -> EPC float32 (complex: float2) values
+template <bool CPLX, bool HALF, int EPC, typename T>
+__device__ __forceinline__ void unpack(uint4 u, T (&v)[EPC])
+{
+    if constexpr (HALF) {
+        const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(h[i]);
+            if constexpr (CPLX) {
+                v[i] = f;
+            } else {
+                v[2 * i] = f.x;
+                v[2 * i + 1] = f.y;
+            }
+        }
+    } else {
+        const T *p = reinterpret_cast<const T *>(&u);
+#pragma unroll
+        for (int i = 0; i < EPC; ++i) v[i] = p[i];
+    }
+}
+
+// acc += w * s (real: w.x * s; complex: complex product, 4 FMA)
+template <bool CPLX, typename T>
+__device__ __forceinline__ void mac(T &acc, float2 w, T s)
+{
+    if constexpr (CPLX) cfma(acc, w, s);
+    else acc = fmaf(w.x, s, acc);
+}
+
+// acc += w0 * (row-0 chunks) + w1 * (row-1 chunks), w1 = wq * fraction,
+// w0 = wq - w1 (IQ: both weights rotated by the entry's phase).  In split
+// mode the lane holds one chunk of row `split_row`.
+template <bool CPLX, bool HALF, bool SPLIT, typename T, int NA, int EPC, int L>
+__device__ __forceinline__ void accumulate(T (&acc)[NA][EPC], float wq, float a, float2 ph,
+                                           const uint4 (&s)[L], int split_row)
 {
     const float w1 = wq * a;
     const float w0 = wq - w1;
+    const float2 W0 = CPLX ? make_float2(w0 * ph.x, w0 * ph.y) : make_float2(w0, 0.f);
+    const float2 W1 = CPLX ? make_float2(w1 * ph.x, w1 * ph.y) : make_float2(w1, 0.f);
+    if constexpr (SPLIT) {
+        const float2 W = split_row ? W1 : W0;
+        T v[EPC];
+        unpack<CPLX, HALF, EPC>(s[0], v);
 #pragma unroll
-    for (int c = 0; c < J; ++c) {
-        if constexpr (CPLX) {
-            const float2 W0 = make_float2(w0 * ph.x, w0 * ph.y);
-            const float2 W1 = make_float2(w1 * ph.x, w1 * ph.y);
-            cfma(acc[c][0], W0, make_float2(s0[c].x, s0[c].y));
-            cfma(acc[c][1], W0, make_float2(s0[c].z, s0[c].w));
-            cfma(acc[c][0], W1, make_float2(s1[c].x, s1[c].y));
-            cfma(acc[c][1], W1, make_float2(s1[c].z, s1[c].w));
-        } else {
-            acc[c][0] = fmaf(w0, s0[c].x, fmaf(w1, s1[c].x, acc[c][0]));
-            acc[c][1] = fmaf(w0, s0[c].y, fmaf(w1, s1[c].y, acc[c][1]));
-            acc[c][2] = fmaf(w0, s0[c].z, fmaf(w1, s1[c].z, acc[c][2]));
-            acc[c][3] = fmaf(w0, s0[c].w, fmaf(w1, s1[c].w, acc[c][3]));
+        for (int e = 0; e < EPC; ++e) mac<CPLX>(acc[0][e], W, v[e]);
+    } else {
+#pragma unroll
+        for (int c = 0; c < NA; ++c) {
+            T v0[EPC], v1[EPC];
+            unpack<CPLX, HALF, EPC>(s[2 * c], v0);
+            unpack<CPLX, HALF, EPC>(s[2 * c + 1], v1);
+#pragma unroll
+            for (int e = 0; e < EPC; ++e) {
+                mac<CPLX>(acc[c][e], W1, v1[e]);
+                mac<CPLX>(acc[c][e], W0, v0[e]);
+            }
         }
     }
 }
@@ -134,20 +191,24 @@ __device__ __forceinline__ void accumulate(T (&acc)[J][CPLX ? 2 : 4], float wq, 
 template <int J, bool CPLX>
 constexpr int min_blocks() { return J >= 4 ? 2 : (J == 2 || CPLX ? 3 : DAS_BRICK_MIN_BLOCKS); }
 
-template <int G, int J, bool CPLX>
+template <int G, int J, bool CPLX, bool HALF, bool SPLIT>
 __global__ void __launch_bounds__(THREADS, min_blocks<J, CPLX>())
-das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__ perm,
+das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict__ perm,
                  const float *__restrict__ tau, const float *__restrict__ wtx,
                  float *__restrict__ out, int bricks_x, int bricks_y, int fb, int q_begin,
                  int q_end, int add_to_out)
 {
+    using LY = Layout<G, J, CPLX, HALF, SPLIT>;
     constexpr int NW = 32 / G;                     // voxels per warp
     constexpr int V = WARPS * NW;                  // voxels per CTA
     constexpr int BX = BrickShape<V>::BX;
-    constexpr int CH = CPLX ? 2 : 4;               // elements per 16-byte chunk
+    constexpr int EPC = LY::EPC;
+    constexpr int L = LY::L;
+    constexpr int NA = LY::NA;
+    constexpr int ROWB = LY::ROWB;
+    constexpr int CPR = ROWB / 16;                 // 16-byte chunks per row
     constexpr int U = J >= 4 ? 1 : (J == 2 ? 2 : DAS_BRICK_U1);   // receivers per loop trip
     constexpr int ES = entry_stride<CPLX>();
-    constexpr int ROWB = 16 * G * J;               // bytes of one row (B * element size)
     using T = typename std::conditional<CPLX, float2, float>::type;
     using E = Entry<CPLX>;
 
@@ -182,16 +243,19 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restric
     const int v0 = warp * NW;
     const int grp = lane / G;
     const int t = lane % G;
+    // pair mode: load 2c + r of a lane is chunk t + G c of row r; split mode: the
+    // lane's one load is chunk t of the row pair (row t / CPR)
     const char *permB = reinterpret_cast<const char *>(perm) + t * 16;
+    const int split_row = SPLIT ? t / CPR : 0;
     const unsigned below = (1u << lane) - 1u;
     const unsigned frac_mask = (1u << fb) - 1u;
     const float frac_scale = (float)(1u << fb);
 
-    T acc[J][CH];
+    T acc[NA][EPC];
 #pragma unroll
-    for (int c = 0; c < J; ++c)
+    for (int c = 0; c < NA; ++c)
 #pragma unroll
-        for (int e = 0; e < CH; ++e) acc[c][e] = T{};
+        for (int e = 0; e < EPC; ++e) acc[c][e] = T{};
 
     for (int m0 = 0; m0 < g.M; m0 += MC) {
         // ---- phase A: distances of the warp's voxels to receiver m0 + lane
@@ -245,8 +309,33 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restric
                 // ---- phase C: this group's list, U entries per trip, pipelined
                 const float wq = tx[(v0 + grp) * g.Q + q].y;
                 const E *ev = eb + grp * ES;
-                // entries -> fractions and row loads of one trip starting at list index i
-                auto load_trip = [&](Trip<U, J, CPLX> &tr, int i) {
+                // entry -> row, fraction (and phase)
+                auto decode = [&](E e, int &row, float &a, float2 &ph) {
+                    if constexpr (CPLX) {
+                        row = __float_as_int(e.x);
+                        a = e.y;
+                        ph = make_float2(e.z, e.w);
+                    } else {
+                        row = base_row + (int)(e >> fb);
+                        // fraction bits placed in a float mantissa of [1, 2), minus 1
+                        a = __int_as_float(0x3f800000 | ((e & frac_mask) << (23 - fb))) - 1.f;
+                        ph = make_float2(1.f, 0.f);
+                    }
+                };
+                // the L 16-byte loads of one entry
+                auto load_rows = [&](int row, uint4 (&s)[L]) {
+                    const char *p0 = permB + (long long)row * ROWB;
+                    if constexpr (SPLIT) {
+                        s[0] = __ldg(reinterpret_cast<const uint4 *>(p0));
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < J; ++c) {
+                            s[2 * c] = __ldg(reinterpret_cast<const uint4 *>(p0 + c * G * 16));
+                            s[2 * c + 1] = __ldg(reinterpret_cast<const uint4 *>(p0 + ROWB + c * G * 16));
+                        }
+                    }
+                };
+                auto load_trip = [&](Trip<U, L> &tr, int i) {
                     E e[U];
                     if constexpr (!CPLX && U % 2 == 0) {
 #pragma unroll
@@ -262,31 +351,18 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restric
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
                         int row;
-                        if constexpr (CPLX) {
-                            row = __float_as_int(e[u].x);
-                            tr.a[u] = e[u].y;
-                            tr.ph[u] = make_float2(e[u].z, e[u].w);
-                        } else {
-                            row = base_row + (int)(e[u] >> fb);
-                            // fraction bits placed in a float mantissa of [1, 2), minus 1
-                            tr.a[u] = __int_as_float(0x3f800000 | ((e[u] & frac_mask) << (23 - fb))) - 1.f;
-                            tr.ph[u] = make_float2(1.f, 0.f);
-                        }
-                        const char *p0 = permB + (long long)row * ROWB;
-#pragma unroll
-                        for (int c = 0; c < J; ++c) {
-                            tr.s0[u][c] = __ldg(reinterpret_cast<const float4 *>(p0 + c * G * 16));
-                            tr.s1[u][c] = __ldg(reinterpret_cast<const float4 *>(p0 + ROWB + c * G * 16));
-                        }
+                        decode(e[u], row, tr.a[u], tr.ph[u]);
+                        load_rows(row, tr.s[u]);
                     }
                 };
-                auto use_trip = [&](const Trip<U, J, CPLX> &tr) {
+                auto use_trip = [&](const Trip<U, L> &tr) {
 #pragma unroll
-                    for (int u = 0; u < U; ++u) accumulate<J, CPLX>(acc, wq, tr.a[u], tr.ph[u], tr.s0[u], tr.s1[u]);
+                    for (int u = 0; u < U; ++u)
+                        accumulate<CPLX, HALF, SPLIT>(acc, wq, tr.a[u], tr.ph[u], tr.s[u], split_row);
                 };
                 int i = 0;
                 if (n_mine >= U) {
-                    Trip<U, J, CPLX> ta, tb;
+                    Trip<U, L> ta, tb;
                     load_trip(ta, 0);
                     i = U;
                     for (;;) {
@@ -301,45 +377,44 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restric
                     }
                 }
                 for (; i < n_mine; ++i) {
-                    Trip<1, J, CPLX> t1;
-                    const E e = ev[i];
                     int row;
-                    if constexpr (CPLX) {
-                        row = __float_as_int(e.x);
-                        t1.a[0] = e.y;
-                        t1.ph[0] = make_float2(e.z, e.w);
-                    } else {
-                        row = base_row + (int)(e >> fb);
-                        t1.a[0] = __int_as_float(0x3f800000 | ((e & frac_mask) << (23 - fb))) - 1.f;
-                        t1.ph[0] = make_float2(1.f, 0.f);
-                    }
-                    const char *p0 = permB + (long long)row * ROWB;
-#pragma unroll
-                    for (int c = 0; c < J; ++c) {
-                        t1.s0[0][c] = __ldg(reinterpret_cast<const float4 *>(p0 + c * G * 16));
-                        t1.s1[0][c] = __ldg(reinterpret_cast<const float4 *>(p0 + ROWB + c * G * 16));
-                    }
-                    accumulate<J, CPLX>(acc, wq, t1.a[0], t1.ph[0], t1.s0[0], t1.s1[0]);
+                    float a;
+                    float2 ph;
+                    uint4 s[L];
+                    decode(ev[i], row, a, ph);
+                    load_rows(row, s);
+                    accumulate<CPLX, HALF, SPLIT>(acc, wq, a, ph, s, split_row);
                 }
                 // the next transmit writes the other buffer; the one after that
                 // comes after the next __syncwarp
             }
         }
-#if DAS_BRICK_CHUNK_BARRIER
-        __syncthreads();
-#endif
     }
 
+    if constexpr (SPLIT) {
+        // add the row-1 half of each chunk (held CPR lanes further on) to row 0
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) {
+            if constexpr (CPLX) {
+                acc[0][e].x += __shfl_xor_sync(0xffffffffu, acc[0][e].x, CPR);
+                acc[0][e].y += __shfl_xor_sync(0xffffffffu, acc[0][e].y, CPR);
+            } else {
+                acc[0][e] += __shfl_xor_sync(0xffffffffu, acc[0][e], CPR);
+            }
+        }
+        if (split_row) return;
+    }
     const int cv = v0 + grp;
     const int cix = bx * BX + cv % BX, ciy = by * (V / BX) + cv / BX;
     if (cix >= g.nx || ciy >= g.ny) return;
     const long long n = cix + (long long)g.nx * (ciy + (long long)g.ny * iz);
     T *outT = reinterpret_cast<T *>(out);
 #pragma unroll
-    for (int c = 0; c < J; ++c)
+    for (int c = 0; c < NA; ++c)
 #pragma unroll
-        for (int e = 0; e < CH; ++e) {
-            T *o = outT + (long long)((t + c * G) * CH + e) * g.N + n;
+        for (int e = 0; e < EPC; ++e) {
+            const int chunk = SPLIT ? t : t + c * G;
+            T *o = outT + (long long)(chunk * EPC + e) * g.N + n;
             if (add_to_out) {
                 T prev = *o;
                 if constexpr (CPLX) *o = make_float2(prev.x + acc[c][e].x, prev.y + acc[c][e].y);
@@ -350,7 +425,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restric
         }
 }
 
-template <int G, int J, bool CPLX>
+template <int G, int J, bool CPLX, bool HALF, bool SPLIT>
 cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
                        const float *w, void *out, cudaStream_t stream, int q0, int q1, bool acc)
 {
@@ -362,52 +437,74 @@ cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, cons
     const long long blocks = (long long)bricks_x * bricks_y * g.nz;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     const size_t smem = smem_bytes<G, CPLX>(g.Q);
-    cudaError_t err = cudaFuncSetAttribute(das_brick_kernel<G, J, CPLX>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kernel = das_brick_kernel<G, J, CPLX, HALF, SPLIT>;
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    das_brick_kernel<G, J, CPLX><<<(int)blocks, THREADS, smem, stream>>>(
-        g, rx, static_cast<const float *>(perm), tau, w, static_cast<float *>(out), bricks_x, bricks_y,
-        fraction_bits(g.K), q0, q1, acc ? 1 : 0);
+    kernel<<<(int)blocks, THREADS, smem, stream>>>(g, rx, perm, tau, w, static_cast<float *>(out),
+                                                   bricks_x, bricks_y, fraction_bits(g.K), q0, q1,
+                                                   acc ? 1 : 0);
     return cudaGetLastError();
 }
 
-bool choose(int B, bool cplx, int &G, int &J)
+// Lanes per voxel G, chunks J, and split mode for B frames.
+//   float32 / complex64 storage: pair mode, CPR = B * size / 16 chunks per row,
+//     G = CPR if <= 8 (J = 1), else G = 8 and J = CPR / 8 in {2, 4};
+//   half / half2 storage: rows of <= 64 bytes (CPR <= 4) use split mode with
+//     G = 2 CPR; wider rows pair mode with G = 8, J = CPR / 8 in {1, 2}.
+bool choose(int B, bool cplx, bool half, int &G, int &J, bool &split)
 {
-    const int ch = cplx ? 2 : 4;
-    if (B % ch != 0) return false;
-    const int chunks = B / ch;
-    if (chunks <= 8) {
-        G = chunks;
+    const int esz = half ? (cplx ? 4 : 2) : (cplx ? 8 : 4);
+    if ((B * esz) % 16 != 0) return false;
+    const int cpr = B * esz / 16;
+    split = false;
+    if (half) {
+        if (cpr <= 4) {
+            split = true;
+            G = 2 * cpr;
+            J = 1;
+            return G == 2 || G == 4 || G == 8;
+        }
+        G = 8;
+        J = cpr / 8;
+        return cpr % 8 == 0 && (J == 1 || J == 2);
+    }
+    if (cpr <= 8) {
+        G = cpr;
         J = 1;
         return G == 2 || G == 4 || G == 8;
     }
     G = 8;
-    J = chunks / 8;
-    return chunks % 8 == 0 && (J == 2 || J == 4);
+    J = cpr / 8;
+    return cpr % 8 == 0 && (J == 2 || J == 4);
 }
 
 }  // namespace
 
-bool brick_supported(int B, bool cplx, int K)
+bool brick_supported(int B, bool cplx, int K, bool half)
 {
     int G, J;
-    return K >= 2 && fraction_bits(K) >= 10 && choose(B, cplx, G, J);
+    bool split;
+    return K >= 2 && fraction_bits(K) >= 10 && choose(B, cplx, half, G, J, split);
 }
 
 cudaError_t launch_brick(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
                          const float *w, void *out, bool cplx, cudaStream_t stream, int q0, int q1,
-                         bool accumulate)
+                         bool accumulate, bool half)
 {
     int G, J;
+    bool split;
     if (q1 < 0) q1 = g.Q;
     if (q0 < 0 || q0 > q1 || q1 > g.Q) return cudaErrorInvalidValue;
-    if (g.K < 2 || !choose(g.B, cplx, G, J)) return cudaErrorInvalidValue;
-#define DAS_BRICK_CASE(GG, JJ)                                                                  \
-    if (G == GG && J == JJ)                                                                     \
-        return cplx ? launch_one<GG, JJ, true>(g, rx, perm, tau, w, out, stream, q0, q1, accumulate) \
-                    : launch_one<GG, JJ, false>(g, rx, perm, tau, w, out, stream, q0, q1, accumulate);
-    DAS_BRICK_CASE(2, 1) DAS_BRICK_CASE(4, 1) DAS_BRICK_CASE(8, 1)
-    DAS_BRICK_CASE(8, 2) DAS_BRICK_CASE(8, 4)
+    if (g.K < 2 || !choose(g.B, cplx, half, G, J, split)) return cudaErrorInvalidValue;
+#define DAS_BRICK_CASE(GG, JJ, HH, SS)                                                         \
+    if (G == GG && J == JJ && half == HH && split == SS)                                       \
+        return cplx ? launch_one<GG, JJ, true, HH, SS>(g, rx, perm, tau, w, out, stream, q0, q1, accumulate) \
+                    : launch_one<GG, JJ, false, HH, SS>(g, rx, perm, tau, w, out, stream, q0, q1, accumulate);
+    DAS_BRICK_CASE(2, 1, false, false) DAS_BRICK_CASE(4, 1, false, false)
+    DAS_BRICK_CASE(8, 1, false, false) DAS_BRICK_CASE(8, 2, false, false)
+    DAS_BRICK_CASE(8, 4, false, false)
+    DAS_BRICK_CASE(2, 1, true, true) DAS_BRICK_CASE(4, 1, true, true) DAS_BRICK_CASE(8, 1, true, true)
+    DAS_BRICK_CASE(8, 1, true, false) DAS_BRICK_CASE(8, 2, true, false)
 #undef DAS_BRICK_CASE
     return cudaErrorInvalidValue;
 }

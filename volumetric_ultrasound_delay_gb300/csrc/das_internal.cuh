@@ -32,19 +32,21 @@ namespace das {
 void record_error(const char *msg);
 
 // Launchers (each returns the cudaError_t of its launch).
-// Permutes the planes of transmits [q0, q1) (q1 < 0: all Q).
+// Permutes the planes of transmits [q0, q1) (q1 < 0: all Q); to_half converts
+// float32 / complex64 elements to half / half2 on the way.
 cudaError_t launch_permute(const void *in, void *out, int elem_bytes, int B, int Q, int M, int K,
-                           int layout, int num_sms, cudaStream_t stream, int q0 = 0, int q1 = -1);
+                           int layout, int num_sms, cudaStream_t stream, int q0 = 0, int q1 = -1,
+                           bool to_half = false);
 cudaError_t launch_bl(const DasGeom &g, const RxPos *rx, const void *rf, const float *tau,
                       const float *w, void *out, bool cplx, cudaStream_t stream);
 bool bi_supported(int B, bool cplx, int group);
 cudaError_t launch_bi(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
                       const float *w, void *out, bool cplx, int group, cudaStream_t stream);
-bool brick_supported(int B, bool cplx, int K);
+bool brick_supported(int B, bool cplx, int K, bool half = false);
 // Sums transmits [q0, q1) (q1 < 0: all Q); with accumulate, adds to out
-// instead of overwriting it.
+// instead of overwriting it; half: perm holds half / half2 samples.
 cudaError_t launch_brick(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
                          const float *w, void *out, bool cplx, cudaStream_t stream, int q0 = 0,
-                         int q1 = -1, bool accumulate = false);
+                         int q1 = -1, bool accumulate = false, bool half = false);
 
 }  // namespace das

@@ -14,6 +14,12 @@
 //   layout 2: out[((q*M + m)*(K+3) + k + 1)*B + b] (Q x M x (K+3) x B: every
 //             (q, m) slab has a row before k = 0 and two rows after k = K-1
 //             that this kernel never writes; the brick kernel keeps them zero)
+//
+// With half-precision storage the copy converts float32 -> half and complex64
+// -> half2 (round to nearest) as it writes: the pages' FP16 variants fuse that
+// conversion into the permute (ffdas paper, Methods, FP16 paragraphs).
+#include <cuda_fp16.h>
+
 #include <cstdint>
 #include <cstring>
 
@@ -26,14 +32,25 @@ constexpr int TILE = 32;
 constexpr int SUB = 2;           // tiles along k per block iteration
 constexpr int THREADS = 256;
 
-template <typename T>
+// element conversion on the way out: identity, or float -> half / float2 -> half2
+// (round to nearest) for half-precision storage of the copy
+template <typename TO, typename TI>
+__device__ __forceinline__ TO convert(TI v) { return v; }
+template <>
+__device__ __forceinline__ __half convert<__half, float>(float v) { return __float2half_rn(v); }
+template <>
+__device__ __forceinline__ __half2 convert<__half2, float2>(float2 v) { return __float22half2_rn(v); }
+
+template <typename T, typename TO>
 __global__ void __launch_bounds__(THREADS)
-permute_kernel(const T *__restrict__ in, T *__restrict__ out, int B, int QM, int K,
+permute_kernel(const T *__restrict__ in, TO *__restrict__ out, int B, int QM, int K,
                long long osk, long long osqm, long long n_blocks, int blocks_b, int blocks_k,
                int vec_in, int vec_out, int qm0)
 {
-    constexpr int V = 16 / sizeof(T);            // elements per 16-byte vector
-    constexpr int VPR = TILE / V;                // vectors per 32-element row
+    constexpr int V = 16 / sizeof(T);            // input elements per 16-byte vector
+    constexpr int VPR = TILE / V;                // input vectors per 32-element row
+    constexpr int VO = 16 / sizeof(TO);          // output elements per 16-byte vector
+    constexpr int VPRO = TILE / VO;              // output vectors per 32-element row
     __shared__ T tile[SUB][TILE][TILE + 1];
     const int tid = threadIdx.x;
 
@@ -76,13 +93,13 @@ permute_kernel(const T *__restrict__ in, T *__restrict__ out, int B, int QM, int
         if (vec_out) {
 #pragma unroll
             for (int s = 0; s < SUB; ++s) {
-                for (int i = tid; i < TILE * VPR; i += THREADS) {
-                    const int krow = i / VPR, v = i % VPR;
-                    const int k = k0 + s * TILE + krow, b = b0 + v * V;
-                    if (k < K && b < B) {   // B % V == 0
-                        T vals[V];
+                for (int i = tid; i < TILE * VPRO; i += THREADS) {
+                    const int krow = i / VPRO, v = i % VPRO;
+                    const int k = k0 + s * TILE + krow, b = b0 + v * VO;
+                    if (k < K && b < B) {   // B % VO == 0
+                        TO vals[VO];
 #pragma unroll
-                        for (int j = 0; j < V; ++j) vals[j] = tile[s][v * V + j][krow];
+                        for (int j = 0; j < VO; ++j) vals[j] = convert<TO>(tile[s][v * VO + j][krow]);
                         uint4 u;
                         memcpy(&u, vals, sizeof(u));
                         *reinterpret_cast<uint4 *>(out + (long long)k * osk + (long long)qm * osqm + b) = u;
@@ -95,23 +112,24 @@ permute_kernel(const T *__restrict__ in, T *__restrict__ out, int B, int QM, int
                     const int krow = i / TILE, bb = i % TILE;
                     const int k = k0 + s * TILE + krow, b = b0 + bb;
                     if (k < K && b < B)
-                        out[(long long)k * osk + (long long)qm * osqm + b] = tile[s][bb][krow];
+                        out[(long long)k * osk + (long long)qm * osqm + b] = convert<TO>(tile[s][bb][krow]);
                 }
         }
         __syncthreads();
     }
 }
 
-template <typename T>
+template <typename T, typename TO = T>
 cudaError_t launch_typed(const void *in, void *out, int B, int Q, int M, int K, int layout,
                          int num_sms, cudaStream_t stream, int q0, int q1)
 {
     constexpr int V = 16 / sizeof(T);
+    constexpr int VO = 16 / sizeof(TO);
     const int QM = Q * M;
     const long long osk = layout == 0 ? (long long)QM * B : (long long)B;
     const long long osqm = layout == 0 ? (long long)B
                          : layout == 1 ? (long long)K * B : (long long)(K + 3) * B;
-    if (layout == 2) out = static_cast<T *>(out) + B;   // row k = 0 of slab 0
+    if (layout == 2) out = static_cast<TO *>(out) + B;   // row k = 0 of slab 0
     const int blocks_b = (B + TILE - 1) / TILE;
     const int blocks_k = (K + TILE * SUB - 1) / (TILE * SUB);
     const long long n_blocks = (long long)(q1 - q0) * M * blocks_b * blocks_k;
@@ -119,11 +137,11 @@ cudaError_t launch_typed(const void *in, void *out, int B, int Q, int M, int K, 
     const bool in_al = (reinterpret_cast<uintptr_t>(in) % 16) == 0;
     const bool out_al = (reinterpret_cast<uintptr_t>(out) % 16) == 0;
     const int vec_in = in_al && (K % V == 0);
-    const int vec_out = out_al && (B % V == 0) && (osk % V == 0) && (osqm % V == 0);
+    const int vec_out = out_al && (B % VO == 0) && (osk % VO == 0) && (osqm % VO == 0);
     const long long cap = (long long)num_sms * 8;
     const int grid = (int)(n_blocks < cap ? n_blocks : cap);
-    permute_kernel<T><<<grid, THREADS, 0, stream>>>(
-        static_cast<const T *>(in), static_cast<T *>(out), B, QM, K, osk, osqm, n_blocks,
+    permute_kernel<T, TO><<<grid, THREADS, 0, stream>>>(
+        static_cast<const T *>(in), static_cast<TO *>(out), B, QM, K, osk, osqm, n_blocks,
         blocks_b, blocks_k, vec_in, vec_out, q0 * M);
     return cudaGetLastError();
 }
@@ -131,10 +149,18 @@ cudaError_t launch_typed(const void *in, void *out, int B, int Q, int M, int K, 
 }  // namespace
 
 cudaError_t launch_permute(const void *in, void *out, int elem_bytes, int B, int Q, int M, int K,
-                           int layout, int num_sms, cudaStream_t stream, int q0, int q1)
+                           int layout, int num_sms, cudaStream_t stream, int q0, int q1,
+                           bool to_half)
 {
     if (q1 < 0) q1 = Q;
     if (q0 < 0 || q0 > q1 || q1 > Q) return cudaErrorInvalidValue;
+    if (to_half) {
+        switch (elem_bytes) {
+        case 4: return launch_typed<float, __half>(in, out, B, Q, M, K, layout, num_sms, stream, q0, q1);
+        case 8: return launch_typed<float2, __half2>(in, out, B, Q, M, K, layout, num_sms, stream, q0, q1);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (elem_bytes) {
     case 2: return launch_typed<unsigned short>(in, out, B, Q, M, K, layout, num_sms, stream, q0, q1);
     case 4: return launch_typed<float>(in, out, B, Q, M, K, layout, num_sms, stream, q0, q1);

@@ -23,7 +23,8 @@ DAS_OK, DAS_ERR_INVALID_ARG, DAS_ERR_UNSUPPORTED, DAS_ERR_OUT_OF_MEMORY, DAS_ERR
 DAS_F32, DAS_C64 = 0, 1
 KERNELS = {"auto": 0, "bl": 1, "bi": 2, "brick": 3}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
-OPT_KERNEL, OPT_DEMOD_HZ, OPT_TIMING, OPT_BI_GROUP, OPT_HOST_GROUPS = 0, 1, 2, 3, 4
+OPT_KERNEL, OPT_DEMOD_HZ, OPT_TIMING, OPT_BI_GROUP, OPT_HOST_GROUPS, OPT_STORAGE = 0, 1, 2, 3, 4, 5
+STORAGE_NATIVE, STORAGE_F16 = 0, 1
 
 # every function the header declares, with its ctypes signature
 _VP = ctypes.c_void_p
@@ -39,7 +40,7 @@ _SIGS = {
     "das_plan_last_times": (_I, [_VP, ctypes.POINTER(_F), ctypes.POINTER(_F)]),
     "das_plan_device_bytes": (_I, [_VP, ctypes.POINTER(ctypes.c_size_t)]),
     "das_plan_destroy": (_I, [_VP]),
-    "das_permute": (_I, [_VP, _VP, _I, _I, _I, _I, _I, _I, _VP]),
+    "das_permute": (_I, [_VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP]),
     "das_beamform_noalloc": (_I, [_VP, _VP, _F, _F, _F, _F, ctypes.c_double, _I, _I, _I, _I, _I,
                                   _VP, _VP, _VP, _VP, _VP]),
     "das_last_error_string": (ctypes.c_char_p, []),
@@ -105,7 +106,7 @@ class Plan:
     """A DAS plan: fixed grid, receivers, physics constants, dtype and sizes."""
 
     def __init__(self, grid, rx_xyz, c, fs, t0=0.0, fnum=0.0, dtype="f32", B=1, Q=1, M=None,
-                 K=1, kernel="auto", f_demod=0.0):
+                 K=1, kernel="auto", f_demod=0.0, storage="native"):
         rx = np.ascontiguousarray(rx_xyz, dtype=np.float32).reshape(-1, 3)
         M = rx.shape[0] if M is None else M
         if M != rx.shape[0]:
@@ -126,6 +127,8 @@ class Plan:
             self.set_option(OPT_KERNEL, KERNELS[kernel])
         if f_demod:
             self.set_option(OPT_DEMOD_HZ, f_demod)
+        if storage != "native":
+            self.set_option(OPT_STORAGE, {"native": STORAGE_NATIVE, "f16": STORAGE_F16}[storage])
 
     # -- options
     def set_option(self, opt: int, value: float):
@@ -209,17 +212,26 @@ class Plan:
             pass
 
 
-def permute(rf, out, layout: int = 0, stream=None):
-    """Bit-exact B x Q x M x K -> K x Q x M x B (layout 0), Q x M x K x B (layout 1)
-    or Q x M x (K+3) x B with sample k at row k + 1 and pad rows untouched (layout 2)."""
+def permute(rf, out, layout: int = 0, stream=None, storage: str = "native"):
+    """B x Q x M x K -> K x Q x M x B (layout 0), Q x M x K x B (layout 1) or
+    Q x M x (K+3) x B with sample k at row k + 1 and pad rows untouched (layout 2).
+    ``storage="native"`` copies bit for bit; ``"f16"`` writes float16 (float32 data)
+    or complex32 as pairs of float16 (complex64 data), ``out`` being a float16
+    tensor with 1 or 2 values per element."""
     import torch
     if rf.dtype not in (torch.float32, torch.complex64) or rf.dim() != 4:
         raise TypeError("rf must be a 4-D float32 or complex64 CUDA tensor")
     B, Q, M, K = rf.shape
     dt = DAS_C64 if rf.dtype == torch.complex64 else DAS_F32
     n_out = B * Q * M * (K + 3 if layout == 2 else K)
-    _check(lib().das_permute(_dev_ptr(rf, "rf"), _dev_ptr(out, "out", rf.dtype, n_out), dt,
-                             B, Q, M, K, layout, _stream_handle(stream)))
+    if storage == "f16":
+        n_out *= 2 if dt == DAS_C64 else 1
+        optr = _dev_ptr(out, "out", torch.float16, n_out)
+    else:
+        optr = _dev_ptr(out, "out", rf.dtype, n_out)
+    st = {"native": STORAGE_NATIVE, "f16": STORAGE_F16}[storage]
+    _check(lib().das_permute(_dev_ptr(rf, "rf"), optr, dt, B, Q, M, K, layout, st,
+                             _stream_handle(stream)))
     return out
 
 
