@@ -31,16 +31,15 @@
 //            contributes (inside the voxel's aperture, a sample inside the
 //            record); a warp ballot compacts each voxel's entries into a dense
 //            list in the warp's own shared memory, and the list lengths stay in
-//            registers.  Lists are double-buffered by transmit parity.  A real
-//            entry is one 32-bit word: the row relative to the first row of
-//            this block of receivers in the high bits, the interpolation
-//            fraction in the low FB bits (FB >= 10; for K = 2048, 15 bits, a
-//            step of 3e-5 samples, 8x finer than float32 resolves f near K);
-//            an IQ entry is {row, fraction, cos, sin} in float32;
+//            registers.  Lists are double-buffered by transmit parity.  An
+//            entry is {row, fraction} (IQ: {row, fraction, cos, sin}) in
+//            float32 bits, so phase C needs no decoding;
 //   phase C: each group walks its voxel's list U entries per trip, software
 //            pipelined: the row loads of the next trip are issued before the
 //            FMAs of the current one, so a warp keeps two trips of loads in
-//            flight; the groups of a warp run independently.
+//            flight; the groups of a warp run independently.  Real data are
+//            accumulated two frames at a time with the packed FP32 FMA of
+//            sm_100+ (__ffma2_rn), halving the FMA instructions.
 #include <cuda_fp16.h>
 
 #include "das_device.cuh"
@@ -73,31 +72,21 @@ struct BrickShape {
     static constexpr int BX = V >= 512 ? 32 : (V >= 128 ? 16 : (V >= 32 ? 8 : 4));
 };
 
-// packed {relative row, fraction} word, or, for IQ, {row, fraction, cos, sin}
+// {row as int bits, fraction} or, for IQ, {row, fraction, cos, sin}
 template <bool CPLX>
-using Entry = typename std::conditional<CPLX, float4, unsigned>::type;
+using Entry = typename std::conditional<CPLX, float4, float2>::type;
 
-// entries per voxel list: MC plus padding, so that a list starts on an 8-byte
-// (IQ: 16-byte) boundary and the lists of a warp's voxels start in different banks
+// entries per voxel list: MC plus padding, so that a list starts on a 16-byte
+// boundary and the lists of a warp's voxels start in different banks
 template <bool CPLX>
 constexpr int entry_stride() { return CPLX ? MC + 1 : MC + 2; }
-
-// fraction bits of a packed entry for records of K samples: the relative row
-// (< 32 (K + 3)) takes the high bits, the fraction the rest (at most 23)
-inline int fraction_bits(int K)
-{
-    const long long span = 32LL * (K + 3);
-    int rel_bits = 0;
-    while ((1LL << rel_bits) < span) ++rel_bits;
-    const int fb = 32 - rel_bits;
-    return fb > 23 ? 23 : fb;
-}
 
 // Storage of the permuted record as seen by one lane of a group.
 //   EPC  elements per 16-byte chunk (float32 4, complex64 2, half 8, half2 4)
 //   ROWB bytes per row (B * element size)
 //   L    16-byte loads per entry and lane
 //   NA   accumulator chunks per lane
+//   NP   float2 accumulators per chunk (real: frame pairs; IQ: one per frame)
 template <int G, int J, bool CPLX, bool HALF, bool SPLIT>
 struct Layout {
     static constexpr int ESZ = HALF ? (CPLX ? 4 : 2) : (CPLX ? 8 : 4);
@@ -105,6 +94,7 @@ struct Layout {
     static constexpr int ROWB = SPLIT ? 8 * G : 16 * G * J;
     static constexpr int L = SPLIT ? 1 : 2 * J;
     static constexpr int NA = SPLIT ? 1 : J;
+    static constexpr int NP = CPLX ? EPC : EPC / 2;
 };
 
 template <int G, bool CPLX>
@@ -123,62 +113,56 @@ struct Trip {
     uint4 s[U][L];
 };
 
-// 16 bytes of samples -> EPC float32 (complex: float2) values
-template <bool CPLX, bool HALF, int EPC, typename T>
-__device__ __forceinline__ void unpack(uint4 u, T (&v)[EPC])
+// 16 bytes of samples -> NP float2 values: pairs of consecutive frames (real)
+// or one complex sample each (IQ), in float32
+template <bool HALF, int NP>
+__device__ __forceinline__ void unpack(uint4 u, float2 (&v)[NP])
 {
     if constexpr (HALF) {
         const __half2 *h = reinterpret_cast<const __half2 *>(&u);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = __half22float2(h[i]);
-            if constexpr (CPLX) {
-                v[i] = f;
-            } else {
-                v[2 * i] = f.x;
-                v[2 * i + 1] = f.y;
-            }
-        }
+        for (int i = 0; i < NP; ++i) v[i] = __half22float2(h[i]);
     } else {
-        const T *p = reinterpret_cast<const T *>(&u);
+        const float2 *p = reinterpret_cast<const float2 *>(&u);
 #pragma unroll
-        for (int i = 0; i < EPC; ++i) v[i] = p[i];
+        for (int i = 0; i < NP; ++i) v[i] = p[i];
     }
 }
 
-// acc += w * s (real: w.x * s; complex: complex product, 4 FMA)
-template <bool CPLX, typename T>
-__device__ __forceinline__ void mac(T &acc, float2 w, T s)
+// acc += w * s: real frame pairs with one packed FMA, complex with four FMAs
+template <bool CPLX>
+__device__ __forceinline__ void mac(float2 &acc, float2 w, float2 s)
 {
     if constexpr (CPLX) cfma(acc, w, s);
-    else acc = fmaf(w.x, s, acc);
+    else acc = __ffma2_rn(w, s, acc);
 }
 
 // acc += w0 * (row-0 chunks) + w1 * (row-1 chunks), w1 = wq * fraction,
-// w0 = wq - w1 (IQ: both weights rotated by the entry's phase).  In split
-// mode the lane holds one chunk of row `split_row`.
-template <bool CPLX, bool HALF, bool SPLIT, typename T, int NA, int EPC, int L>
-__device__ __forceinline__ void accumulate(T (&acc)[NA][EPC], float wq, float a, float2 ph,
+// w0 = wq - w1 (IQ: both weights rotated by the entry's phase; real: the
+// weight broadcast to both frames of a pair).  In split mode the lane holds
+// one chunk of row `split_row`.
+template <bool CPLX, bool HALF, bool SPLIT, int NA, int NP, int L>
+__device__ __forceinline__ void accumulate(float2 (&acc)[NA][NP], float wq, float a, float2 ph,
                                            const uint4 (&s)[L], int split_row)
 {
     const float w1 = wq * a;
     const float w0 = wq - w1;
-    const float2 W0 = CPLX ? make_float2(w0 * ph.x, w0 * ph.y) : make_float2(w0, 0.f);
-    const float2 W1 = CPLX ? make_float2(w1 * ph.x, w1 * ph.y) : make_float2(w1, 0.f);
+    const float2 W0 = CPLX ? make_float2(w0 * ph.x, w0 * ph.y) : make_float2(w0, w0);
+    const float2 W1 = CPLX ? make_float2(w1 * ph.x, w1 * ph.y) : make_float2(w1, w1);
     if constexpr (SPLIT) {
         const float2 W = split_row ? W1 : W0;
-        T v[EPC];
-        unpack<CPLX, HALF, EPC>(s[0], v);
+        float2 v[NP];
+        unpack<HALF, NP>(s[0], v);
 #pragma unroll
-        for (int e = 0; e < EPC; ++e) mac<CPLX>(acc[0][e], W, v[e]);
+        for (int e = 0; e < NP; ++e) mac<CPLX>(acc[0][e], W, v[e]);
     } else {
 #pragma unroll
         for (int c = 0; c < NA; ++c) {
-            T v0[EPC], v1[EPC];
-            unpack<CPLX, HALF, EPC>(s[2 * c], v0);
-            unpack<CPLX, HALF, EPC>(s[2 * c + 1], v1);
+            float2 v0[NP], v1[NP];
+            unpack<HALF, NP>(s[2 * c], v0);
+            unpack<HALF, NP>(s[2 * c + 1], v1);
 #pragma unroll
-            for (int e = 0; e < EPC; ++e) {
+            for (int e = 0; e < NP; ++e) {
                 mac<CPLX>(acc[c][e], W1, v1[e]);
                 mac<CPLX>(acc[c][e], W0, v0[e]);
             }
@@ -195,21 +179,21 @@ template <int G, int J, bool CPLX, bool HALF, bool SPLIT>
 __global__ void __launch_bounds__(THREADS, min_blocks<J, CPLX>())
 das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict__ perm,
                  const float *__restrict__ tau, const float *__restrict__ wtx,
-                 float *__restrict__ out, int bricks_x, int bricks_y, int fb, int q_begin,
-                 int q_end, int add_to_out)
+                 float *__restrict__ out, int bricks_x, int bricks_y, int q_begin, int q_end,
+                 int add_to_out)
 {
     using LY = Layout<G, J, CPLX, HALF, SPLIT>;
     constexpr int NW = 32 / G;                     // voxels per warp
     constexpr int V = WARPS * NW;                  // voxels per CTA
     constexpr int BX = BrickShape<V>::BX;
     constexpr int EPC = LY::EPC;
+    constexpr int NP = LY::NP;
     constexpr int L = LY::L;
     constexpr int NA = LY::NA;
     constexpr int ROWB = LY::ROWB;
     constexpr int CPR = ROWB / 16;                 // 16-byte chunks per row
     constexpr int U = J >= 4 ? 1 : (J == 2 ? 2 : DAS_BRICK_U1);   // receivers per loop trip
     constexpr int ES = entry_stride<CPLX>();
-    using T = typename std::conditional<CPLX, float2, float>::type;
     using E = Entry<CPLX>;
 
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -219,10 +203,12 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
     E *ent = reinterpret_cast<E *>(smem_raw) + warp * (2 * NW * ES);        // this warp's [2][NW][ES]
     float2 *tx = reinterpret_cast<float2 *>(reinterpret_cast<E *>(smem_raw) + 2 * V * ES);  // [V][Q]
 
+    // deepest slice first: deep voxels have the widest apertures and the most
+    // work, so launching them first leaves the light shallow bricks for the tail
     const int bx = blockIdx.x % bricks_x;
     const int rb = blockIdx.x / bricks_x;
     const int by = rb % bricks_y;
-    const int iz = rb / bricks_y;
+    const int iz = g.nz - 1 - rb / bricks_y;
     const int KP = g.K + 3;                        // rows per padded slab
 
     // ---- per-voxel transmit delay (samples) and weight, once per CTA
@@ -248,14 +234,12 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
     const char *permB = reinterpret_cast<const char *>(perm) + t * 16;
     const int split_row = SPLIT ? t / CPR : 0;
     const unsigned below = (1u << lane) - 1u;
-    const unsigned frac_mask = (1u << fb) - 1u;
-    const float frac_scale = (float)(1u << fb);
 
-    T acc[NA][EPC];
+    float2 acc[NA][NP];
 #pragma unroll
     for (int c = 0; c < NA; ++c)
 #pragma unroll
-        for (int e = 0; e < EPC; ++e) acc[c][e] = T{};
+        for (int e = 0; e < NP; ++e) acc[c][e] = make_float2(0.f, 0.f);
 
     for (int m0 = 0; m0 < g.M; m0 += MC) {
         // ---- phase A: distances of the warp's voxels to receiver m0 + lane
@@ -291,14 +275,14 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                     const bool ok = (fl >= -1.f) && (fl <= (float)(g.K - 1));
                     const unsigned bal = __ballot_sync(0xffffffffu, ok);
                     if (ok) {
-                        const int rel = lane * KP + (int)fl + 1;  // row within this block
+                        const int row = base_row + lane * KP + (int)fl + 1;
                         const float a = f - fl;                   // in [0, 1)
                         E e;
                         if constexpr (CPLX) {
                             const float2 ph = demod_phase(g, f);
-                            e = make_float4(__int_as_float(base_row + rel), a, ph.x, ph.y);
+                            e = make_float4(__int_as_float(row), a, ph.x, ph.y);
                         } else {
-                            e = ((unsigned)rel << fb) | __float2uint_rz(a * frac_scale);
+                            e = make_float2(__int_as_float(row), a);
                         }
                         eb[i * ES + __popc(bal & below)] = e;
                     }
@@ -311,16 +295,10 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                 const E *ev = eb + grp * ES;
                 // entry -> row, fraction (and phase)
                 auto decode = [&](E e, int &row, float &a, float2 &ph) {
-                    if constexpr (CPLX) {
-                        row = __float_as_int(e.x);
-                        a = e.y;
-                        ph = make_float2(e.z, e.w);
-                    } else {
-                        row = base_row + (int)(e >> fb);
-                        // fraction bits placed in a float mantissa of [1, 2), minus 1
-                        a = __int_as_float(0x3f800000 | ((e & frac_mask) << (23 - fb))) - 1.f;
-                        ph = make_float2(1.f, 0.f);
-                    }
+                    row = __float_as_int(e.x);
+                    a = e.y;
+                    if constexpr (CPLX) ph = make_float2(e.z, e.w);
+                    else ph = make_float2(1.f, 0.f);
                 };
                 // the L 16-byte loads of one entry
                 auto load_rows = [&](int row, uint4 (&s)[L]) {
@@ -338,11 +316,12 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                 auto load_trip = [&](Trip<U, L> &tr, int i) {
                     E e[U];
                     if constexpr (!CPLX && U % 2 == 0) {
+                        // two 8-byte entries per 16-byte shared load
 #pragma unroll
                         for (int u = 0; u < U; u += 2) {
-                            const uint2 two = *reinterpret_cast<const uint2 *>(ev + i + u);
-                            e[u] = two.x;
-                            e[u + 1] = two.y;
+                            const float4 two = *reinterpret_cast<const float4 *>(ev + i + u);
+                            e[u] = make_float2(two.x, two.y);
+                            e[u + 1] = make_float2(two.z, two.w);
                         }
                     } else {
 #pragma unroll
@@ -394,13 +373,9 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
     if constexpr (SPLIT) {
         // add the row-1 half of each chunk (held CPR lanes further on) to row 0
 #pragma unroll
-        for (int e = 0; e < EPC; ++e) {
-            if constexpr (CPLX) {
-                acc[0][e].x += __shfl_xor_sync(0xffffffffu, acc[0][e].x, CPR);
-                acc[0][e].y += __shfl_xor_sync(0xffffffffu, acc[0][e].y, CPR);
-            } else {
-                acc[0][e] += __shfl_xor_sync(0xffffffffu, acc[0][e], CPR);
-            }
+        for (int e = 0; e < NP; ++e) {
+            acc[0][e].x += __shfl_xor_sync(0xffffffffu, acc[0][e].x, CPR);
+            acc[0][e].y += __shfl_xor_sync(0xffffffffu, acc[0][e].y, CPR);
         }
         if (split_row) return;
     }
@@ -408,19 +383,20 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
     const int cix = bx * BX + cv % BX, ciy = by * (V / BX) + cv / BX;
     if (cix >= g.nx || ciy >= g.ny) return;
     const long long n = cix + (long long)g.nx * (ciy + (long long)g.ny * iz);
-    T *outT = reinterpret_cast<T *>(out);
 #pragma unroll
     for (int c = 0; c < NA; ++c)
 #pragma unroll
         for (int e = 0; e < EPC; ++e) {
             const int chunk = SPLIT ? t : t + c * G;
-            T *o = outT + (long long)(chunk * EPC + e) * g.N + n;
-            if (add_to_out) {
-                T prev = *o;
-                if constexpr (CPLX) *o = make_float2(prev.x + acc[c][e].x, prev.y + acc[c][e].y);
-                else *o = prev + acc[c][e];
+            const long long idx = (long long)(chunk * EPC + e) * g.N + n;
+            if constexpr (CPLX) {
+                float2 *o = reinterpret_cast<float2 *>(out) + idx;
+                const float2 v = acc[c][e];
+                *o = add_to_out ? make_float2(o->x + v.x, o->y + v.y) : v;
             } else {
-                *o = acc[c][e];
+                float *o = out + idx;
+                const float v = (e & 1) ? acc[c][e >> 1].y : acc[c][e >> 1].x;
+                *o = add_to_out ? *o + v : v;
             }
         }
 }
@@ -441,8 +417,7 @@ cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, cons
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     kernel<<<(int)blocks, THREADS, smem, stream>>>(g, rx, perm, tau, w, static_cast<float *>(out),
-                                                   bricks_x, bricks_y, fraction_bits(g.K), q0, q1,
-                                                   acc ? 1 : 0);
+                                                   bricks_x, bricks_y, q0, q1, acc ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -484,7 +459,7 @@ bool brick_supported(int B, bool cplx, int K, bool half)
 {
     int G, J;
     bool split;
-    return K >= 2 && fraction_bits(K) >= 10 && choose(B, cplx, half, G, J, split);
+    return K >= 2 && choose(B, cplx, half, G, J, split);
 }
 
 cudaError_t launch_brick(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
