@@ -31,9 +31,8 @@
 //            contributes (inside the voxel's aperture, a sample inside the
 //            record); a warp ballot compacts each voxel's entries into a dense
 //            list in the warp's own shared memory, and the list lengths stay in
-//            registers.  Lists are double-buffered by transmit parity.  An
-//            entry is {row, fraction} (IQ: {row, fraction, cos, sin}) in
-//            float32 bits, so phase C needs no decoding;
+//            registers.  Lists are double-buffered by transmit parity (entry
+//            formats below);
 //   phase C: each group walks its voxel's list U entries per trip, software
 //            pipelined: the row loads of the next trip are issued before the
 //            FMAs of the current one, so a warp keeps two trips of loads in
@@ -44,17 +43,20 @@
 
 #include "das_device.cuh"
 
-// tuning: receivers per phase-C trip when a lane holds one chunk (J = 1), the
-// CTAs per SM the register allocation must allow for real records with J = 1,
-// and the warps per CTA
+// tuning (float32 storage, one chunk per lane): receivers per phase-C trip
+// and the CTAs per SM the register allocation must allow; half storage keeps
+// 2 receivers per trip and 5 CTAs per SM; and the warps per CTA
 #ifndef DAS_BRICK_U1
-#define DAS_BRICK_U1 2
+#define DAS_BRICK_U1 4
 #endif
 #ifndef DAS_BRICK_MIN_BLOCKS
-#define DAS_BRICK_MIN_BLOCKS 5
+#define DAS_BRICK_MIN_BLOCKS 4
 #endif
 #ifndef DAS_BRICK_WARPS
 #define DAS_BRICK_WARPS 8
+#endif
+#ifndef DAS_BRICK_PACKED
+#define DAS_BRICK_PACKED 1     // real entries packed into 32 bits (else {row, fraction} floats)
 #endif
 
 namespace das {
@@ -72,14 +74,35 @@ struct BrickShape {
     static constexpr int BX = V >= 512 ? 32 : (V >= 128 ? 16 : (V >= 32 ? 8 : 4));
 };
 
-// {row as int bits, fraction} or, for IQ, {row, fraction, cos, sin}
-template <bool CPLX>
-using Entry = typename std::conditional<CPLX, float4, float2>::type;
+// Real entry: one 32-bit word, the row relative to the first row of the block
+// of receivers in the high bits and the interpolation fraction in the low FB
+// bits (FB >= 10; for K = 2048, 15 bits, a step of 3e-5 samples, 8x finer
+// than float32 resolves f near K) -- or {row, fraction} in float32 bits.
+// IQ entry: {row, fraction, cos, sin} in float32 bits.  Real entries are
+// packed for float32 storage, whose phase C is bound by shared-memory and L1
+// traffic; half storage moves half the bytes and keeps the undecoded floats.
+template <bool CPLX, bool HALF>
+constexpr bool packed_entries() { return !CPLX && !HALF && DAS_BRICK_PACKED != 0; }
+template <bool CPLX, bool HALF>
+using Entry = typename std::conditional<CPLX, float4,
+                                        typename std::conditional<packed_entries<CPLX, HALF>(),
+                                                                  unsigned, float2>::type>::type;
 
 // entries per voxel list: MC plus padding, so that a list starts on a 16-byte
 // boundary and the lists of a warp's voxels start in different banks
 template <bool CPLX>
 constexpr int entry_stride() { return CPLX ? MC + 1 : MC + 2; }
+
+// fraction bits of a packed entry for records of K samples: the relative row
+// (< 32 (K + 3)) takes the high bits, the fraction the rest (at most 23)
+inline int fraction_bits(int K)
+{
+    const long long span = 32LL * (K + 3);
+    int rel_bits = 0;
+    while ((1LL << rel_bits) < span) ++rel_bits;
+    const int fb = 32 - rel_bits;
+    return fb > 23 ? 23 : fb;
+}
 
 // Storage of the permuted record as seen by one lane of a group.
 //   EPC  elements per 16-byte chunk (float32 4, complex64 2, half 8, half2 4)
@@ -97,11 +120,11 @@ struct Layout {
     static constexpr int NP = CPLX ? EPC : EPC / 2;
 };
 
-template <int G, bool CPLX>
+template <int G, bool CPLX, bool HALF>
 size_t smem_bytes(int Q)
 {
     constexpr int V = WARPS * (32 / G);
-    return sizeof(Entry<CPLX>) * 2 * V * entry_stride<CPLX>() + sizeof(float2) * (size_t)V * Q;
+    return sizeof(Entry<CPLX, HALF>) * 2 * V * entry_stride<CPLX>() + sizeof(float2) * (size_t)V * Q;
 }
 
 // One pipelined trip of phase C: U entries, their fractions (and phases) and
@@ -172,15 +195,22 @@ __device__ __forceinline__ void accumulate(float2 (&acc)[NA][NP], float wq, floa
 
 // CTAs per SM the register allocation must allow: lanes that hold more chunks
 // (J) or complex samples keep more row data in flight per trip
-template <int J, bool CPLX>
-constexpr int min_blocks() { return J >= 4 ? 2 : (J == 2 || CPLX ? 3 : DAS_BRICK_MIN_BLOCKS); }
+template <int J, bool CPLX, bool HALF>
+constexpr int min_blocks()
+{
+    return J >= 4 ? 2 : (J == 2 || CPLX ? 3 : (HALF ? 5 : DAS_BRICK_MIN_BLOCKS));
+}
+
+// receivers per phase-C trip
+template <int J, bool HALF>
+constexpr int trip_size() { return J >= 4 ? 1 : (J == 2 ? 2 : (HALF ? 2 : DAS_BRICK_U1)); }
 
 template <int G, int J, bool CPLX, bool HALF, bool SPLIT>
-__global__ void __launch_bounds__(THREADS, min_blocks<J, CPLX>())
+__global__ void __launch_bounds__(THREADS, min_blocks<J, CPLX, HALF>())
 das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict__ perm,
                  const float *__restrict__ tau, const float *__restrict__ wtx,
-                 float *__restrict__ out, int bricks_x, int bricks_y, int q_begin, int q_end,
-                 int add_to_out)
+                 float *__restrict__ out, int bricks_x, int bricks_y, int fb, int q_begin,
+                 int q_end, int add_to_out)
 {
     using LY = Layout<G, J, CPLX, HALF, SPLIT>;
     constexpr int NW = 32 / G;                     // voxels per warp
@@ -192,9 +222,10 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
     constexpr int NA = LY::NA;
     constexpr int ROWB = LY::ROWB;
     constexpr int CPR = ROWB / 16;                 // 16-byte chunks per row
-    constexpr int U = J >= 4 ? 1 : (J == 2 ? 2 : DAS_BRICK_U1);   // receivers per loop trip
+    constexpr int U = trip_size<J, HALF>();        // receivers per loop trip
     constexpr int ES = entry_stride<CPLX>();
-    using E = Entry<CPLX>;
+    using E = Entry<CPLX, HALF>;
+    constexpr bool PACKED = packed_entries<CPLX, HALF>();
 
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int tid = threadIdx.x;
@@ -234,6 +265,8 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
     const char *permB = reinterpret_cast<const char *>(perm) + t * 16;
     const int split_row = SPLIT ? t / CPR : 0;
     const unsigned below = (1u << lane) - 1u;
+    const unsigned frac_mask = (1u << fb) - 1u;
+    const float frac_scale = (float)(1u << fb);
 
     float2 acc[NA][NP];
 #pragma unroll
@@ -275,14 +308,16 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                     const bool ok = (fl >= -1.f) && (fl <= (float)(g.K - 1));
                     const unsigned bal = __ballot_sync(0xffffffffu, ok);
                     if (ok) {
-                        const int row = base_row + lane * KP + (int)fl + 1;
+                        const int rel = lane * KP + (int)fl + 1;  // row within this block
                         const float a = f - fl;                   // in [0, 1)
                         E e;
                         if constexpr (CPLX) {
                             const float2 ph = demod_phase(g, f);
-                            e = make_float4(__int_as_float(row), a, ph.x, ph.y);
+                            e = make_float4(__int_as_float(base_row + rel), a, ph.x, ph.y);
+                        } else if constexpr (PACKED) {
+                            e = ((unsigned)rel << fb) | __float2uint_rz(a * frac_scale);
                         } else {
-                            e = make_float2(__int_as_float(row), a);
+                            e = make_float2(__int_as_float(base_row + rel), a);
                         }
                         eb[i * ES + __popc(bal & below)] = e;
                     }
@@ -295,10 +330,17 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                 const E *ev = eb + grp * ES;
                 // entry -> row, fraction (and phase)
                 auto decode = [&](E e, int &row, float &a, float2 &ph) {
-                    row = __float_as_int(e.x);
-                    a = e.y;
-                    if constexpr (CPLX) ph = make_float2(e.z, e.w);
-                    else ph = make_float2(1.f, 0.f);
+                    if constexpr (!CPLX && PACKED) {
+                        row = base_row + (int)(e >> fb);
+                        // fraction bits placed in a float mantissa of [1, 2), minus 1
+                        a = __int_as_float(0x3f800000 | ((e & frac_mask) << (23 - fb))) - 1.f;
+                        ph = make_float2(1.f, 0.f);
+                    } else {
+                        row = __float_as_int(e.x);
+                        a = e.y;
+                        if constexpr (CPLX) ph = make_float2(e.z, e.w);
+                        else ph = make_float2(1.f, 0.f);
+                    }
                 };
                 // the L 16-byte loads of one entry
                 auto load_rows = [&](int row, uint4 (&s)[L]) {
@@ -315,7 +357,15 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                 };
                 auto load_trip = [&](Trip<U, L> &tr, int i) {
                     E e[U];
-                    if constexpr (!CPLX && U % 2 == 0) {
+                    if constexpr (!CPLX && PACKED && U % 2 == 0) {
+                        // two 4-byte entries per 8-byte shared load
+#pragma unroll
+                        for (int u = 0; u < U; u += 2) {
+                            const uint2 two = *reinterpret_cast<const uint2 *>(ev + i + u);
+                            e[u] = two.x;
+                            e[u + 1] = two.y;
+                        }
+                    } else if constexpr (!CPLX && !PACKED && U % 2 == 0) {
                         // two 8-byte entries per 16-byte shared load
 #pragma unroll
                         for (int u = 0; u < U; u += 2) {
@@ -412,12 +462,13 @@ cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, cons
     const int bricks_y = (g.ny + BY - 1) / BY;
     const long long blocks = (long long)bricks_x * bricks_y * g.nz;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    const size_t smem = smem_bytes<G, CPLX>(g.Q);
+    const size_t smem = smem_bytes<G, CPLX, HALF>(g.Q);
     auto kernel = das_brick_kernel<G, J, CPLX, HALF, SPLIT>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     kernel<<<(int)blocks, THREADS, smem, stream>>>(g, rx, perm, tau, w, static_cast<float *>(out),
-                                                   bricks_x, bricks_y, q0, q1, acc ? 1 : 0);
+                                                   bricks_x, bricks_y, fraction_bits(g.K), q0, q1,
+                                                   acc ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -459,7 +510,7 @@ bool brick_supported(int B, bool cplx, int K, bool half)
 {
     int G, J;
     bool split;
-    return K >= 2 && choose(B, cplx, half, G, J, split);
+    return K >= 2 && fraction_bits(K) >= 10 && choose(B, cplx, half, G, J, split);
 }
 
 cudaError_t launch_brick(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
