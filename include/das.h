@@ -133,6 +133,21 @@ das_status das_plan_create(das_plan *plan, const das_grid *grid, const float *rx
                            float c, float fs, float t0, float fnum, das_dtype dtype,
                            int B, int Q, int M, int K);
 
+/*
+ * Plan over an explicit list of voxel positions instead of a regular grid: the
+ * sparse-voxel form of the operation (ffdas docs, "How It Works", das_sparse
+ * in "Mixed-precision storage" and "Other operations").  y and the Q x N
+ * tau_tx / w_tx arrays are indexed by list position n.
+ *   voxel_xyz  host, N x 3 float32 positions (metres), copied.
+ *   other arguments as das_plan_create.
+ * The brick kernel takes bricks of consecutive list entries, so ordering the
+ * list so that neighbours in it are neighbours in space keeps its caches warm.
+ * Errors: as das_plan_create.
+ */
+das_status das_plan_create_points(das_plan *plan, const float *voxel_xyz, int N,
+                                  const float *rx_xyz, float c, float fs, float t0, float fnum,
+                                  das_dtype dtype, int B, int Q, int M, int K);
+
 /* Sets / reads one das_option.  Errors: DAS_ERR_INVALID_ARG (null plan, unknown
  * option or value), DAS_ERR_UNSUPPORTED (see DAS_OPT_DEMOD_HZ). */
 das_status das_plan_set_option(das_plan plan, int option, double value);

@@ -52,6 +52,7 @@ struct das_plan_s {
     bool last_had_permute = false;
     cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
     RxPos *d_rx = nullptr;
+    float4 *d_vox = nullptr;                  // voxel list (sample units), list plans only
     void *d_perm = nullptr;
     size_t perm_bytes = 0;
     bool perm_pads_zero = false;   // scratch holds the padded layout with zero pad rows
@@ -109,6 +110,7 @@ das_status check_supported(const das_plan_s *p, int kernel)
 void release(das_plan_s *p)
 {
     cudaFree(p->d_rx);
+    cudaFree(p->d_vox);
     cudaFree(p->d_perm);
     cudaFree(p->d_rf);
     cudaFree(p->d_out);
@@ -234,6 +236,42 @@ das_status das_plan_create(das_plan *plan, const das_grid *grid, const float *rx
         return cuda_fail(e, "receiver upload");
     }
     *plan = p;
+    return DAS_OK;
+}
+
+das_status das_plan_create_points(das_plan *plan, const float *voxel_xyz, int N,
+                                  const float *rx_xyz, float c, float fs, float t0, float fnum,
+                                  das_dtype dtype, int B, int Q, int M, int K)
+{
+    g_err[0] = '\0';
+    if (!plan) return fail(DAS_ERR_INVALID_ARG, "plan is NULL");
+    *plan = nullptr;
+    if (!voxel_xyz) return fail(DAS_ERR_INVALID_ARG, "voxel_xyz is NULL");
+    if (N < 1) return fail(DAS_ERR_INVALID_ARG, "N must be >= 1");
+    if (!(c > 0.f) || !(fs > 0.f) || !std::isfinite(c) || !std::isfinite(fs))
+        return fail(DAS_ERR_INVALID_ARG, "c and fs must be > 0");
+    for (long long i = 0; i < 3LL * N; ++i)
+        if (!std::isfinite(voxel_xyz[i])) return fail(DAS_ERR_INVALID_ARG, "voxel position not finite");
+    // a 1 x 1 x N grid carries the sizes; the positions come from the list
+    const das_grid grid = {1, 1, N, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    das_status st = das_plan_create(plan, &grid, rx_xyz, c, fs, t0, fnum, dtype, B, Q, M, K);
+    if (st != DAS_OK) return st;
+    das_plan_s *p = *plan;
+    const double s = (double)fs / (double)c;
+    std::vector<float4> hv(N);
+    for (int n = 0; n < N; ++n)
+        hv[n] = make_float4((float)(voxel_xyz[3 * n] * s), (float)(voxel_xyz[3 * n + 1] * s),
+                            (float)(voxel_xyz[3 * n + 2] * s), 0.f);
+    cudaError_t e = cudaMalloc(&p->d_vox, sizeof(float4) * (size_t)N);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(p->d_vox, hv.data(), sizeof(float4) * (size_t)N, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+        das_plan_destroy(p);
+        *plan = nullptr;
+        cudaGetLastError();
+        return cuda_fail(e, "voxel list upload");
+    }
+    p->geom.vox = p->d_vox;
     return DAS_OK;
 }
 
@@ -464,7 +502,7 @@ das_status das_plan_last_times(das_plan p, float *permute_ms, float *das_ms)
 das_status das_plan_device_bytes(das_plan p, size_t *bytes)
 {
     if (!p || !bytes) return fail(DAS_ERR_INVALID_ARG, "NULL argument");
-    size_t b = sizeof(RxPos) * p->M + p->perm_bytes;
+    size_t b = sizeof(RxPos) * p->M + p->perm_bytes + (p->d_vox ? sizeof(float4) * (size_t)p->N : 0);
     if (p->d_rf) b += p->rf_bytes();
     if (p->d_out) b += p->out_bytes();
     if (p->d_tau) b += p->txw_bytes();

@@ -234,21 +234,39 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
     E *ent = reinterpret_cast<E *>(smem_raw) + warp * (2 * NW * ES);        // this warp's [2][NW][ES]
     float2 *tx = reinterpret_cast<float2 *>(reinterpret_cast<E *>(smem_raw) + 2 * V * ES);  // [V][Q]
 
-    // deepest slice first: deep voxels have the widest apertures and the most
-    // work, so launching them first leaves the light shallow bricks for the tail
+    // Grid: brick (bx, by, iz), deepest slice first (deep voxels have the
+    // widest apertures and the most work, so launching them first leaves the
+    // light shallow bricks for the tail).  Voxel list: V consecutive entries.
     const int bx = blockIdx.x % bricks_x;
     const int rb = blockIdx.x / bricks_x;
     const int by = rb % bricks_y;
     const int iz = g.nz - 1 - rb / bricks_y;
     const int KP = g.K + 3;                        // rows per padded slab
+    // voxel v of this CTA: its index n (false if the brick hangs over the grid
+    // or the list) and, on request, its position in sample units
+    auto voxel = [&](int v, int &n, float3 *pos) -> bool {
+        if (g.vox) {
+            n = blockIdx.x * V + v;
+            if (n >= g.N) return false;
+            if (pos) {
+                const float4 p = __ldg(g.vox + n);
+                *pos = make_float3(p.x, p.y, p.z);
+            }
+            return true;
+        }
+        const int ix = bx * BX + v % BX, iy = by * (V / BX) + v / BX;
+        if (ix >= g.nx || iy >= g.ny) return false;
+        n = ix + g.nx * (iy + g.ny * iz);
+        if (pos) *pos = voxel_position(g, ix, iy, iz);
+        return true;
+    };
 
     // ---- per-voxel transmit delay (samples) and weight, once per CTA
     for (int e = tid; e < V * g.Q; e += THREADS) {
         const int v = e / g.Q, q = e % g.Q;
-        const int ix = bx * BX + v % BX, iy = by * (V / BX) + v / BX;
         float2 val = make_float2(0.f, 0.f);
-        if (ix < g.nx && iy < g.ny) {
-            const long long n = ix + (long long)g.nx * (iy + (long long)g.ny * iz);
+        int n;
+        if (voxel(v, n, nullptr)) {
             val.x = fmaf(__ldg(tau + (long long)q * g.N + n), g.fs, -g.t0fs);
             val.y = __ldg(wtx + (long long)q * g.N + n);
         }
@@ -282,12 +300,12 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
         bool any = false;
 #pragma unroll
         for (int i = 0; i < NW; ++i) {
-            const int v = v0 + i;
-            const int ix = bx * BX + v % BX, iy = by * (V / BX) + v / BX;
             dist[i] = FAR;
-            if (m < g.M && ix < g.nx && iy < g.ny) {
+            int n;
+            float3 pos;
+            if (m < g.M && voxel(v0 + i, n, &pos)) {
                 float d;
-                if (receive_geometry(g, voxel_position(g, ix, iy, iz), r, d)) {
+                if (receive_geometry(g, pos, r, d)) {
                     dist[i] = d;
                     any = true;
                 }
@@ -429,10 +447,8 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
         }
         if (split_row) return;
     }
-    const int cv = v0 + grp;
-    const int cix = bx * BX + cv % BX, ciy = by * (V / BX) + cv / BX;
-    if (cix >= g.nx || ciy >= g.ny) return;
-    const long long n = cix + (long long)g.nx * (ciy + (long long)g.ny * iz);
+    int n;
+    if (!voxel(v0 + grp, n, nullptr)) return;
 #pragma unroll
     for (int c = 0; c < NA; ++c)
 #pragma unroll
@@ -458,9 +474,9 @@ cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, cons
     constexpr int V = WARPS * (32 / G);
     constexpr int BX = BrickShape<V>::BX;
     constexpr int BY = V / BX;
-    const int bricks_x = (g.nx + BX - 1) / BX;
-    const int bricks_y = (g.ny + BY - 1) / BY;
-    const long long blocks = (long long)bricks_x * bricks_y * g.nz;
+    const int bricks_x = g.vox ? (g.N + V - 1) / V : (g.nx + BX - 1) / BX;
+    const int bricks_y = g.vox ? 1 : (g.ny + BY - 1) / BY;
+    const long long blocks = (long long)bricks_x * bricks_y * (g.vox ? 1 : g.nz);
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     const size_t smem = smem_bytes<G, CPLX, HALF>(g.Q);
     auto kernel = das_brick_kernel<G, J, CPLX, HALF, SPLIT>;

@@ -13,6 +13,10 @@ namespace das {
 
 __device__ __forceinline__ float3 voxel_position(const DasGeom &g, int n)
 {
+    if (g.vox) {
+        const float4 p = __ldg(g.vox + n);
+        return make_float3(p.x, p.y, p.z);
+    }
     const int ix = n % g.nx;
     const int r = n / g.nx;
     const int iy = r % g.ny;

@@ -11,7 +11,7 @@
 // delay in samples and the fractional index is f = tau_tx * fs - t0 * fs + d.
 struct DasGeom {
     int nx, ny, nz;
-    int N;                // nx * ny * nz
+    int N;                // nx * ny * nz, or the length of the voxel list
     float x0, y0, z0;     // first voxel, sample units
     float dx, dy, dz;     // grid spacing, sample units
     float fs;             // Hz, converts tau_tx (s) to samples
@@ -21,6 +21,7 @@ struct DasGeom {
     float fd_over_fs;     // demodulation cycles per sample (IQ)
     int rotate;           // 1: apply the IQ phase
     int B, Q, M, K;
+    const float4 *vox;    // voxel list (sample units), or nullptr for the regular grid
 };
 
 // Receiver record of the plan: position in sample units.

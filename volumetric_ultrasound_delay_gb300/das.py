@@ -32,6 +32,7 @@ _I = ctypes.c_int
 _F = ctypes.c_float
 _SIGS = {
     "das_plan_create": (_I, [ctypes.POINTER(_VP), _VP, _VP, _F, _F, _F, _F, _I, _I, _I, _I, _I]),
+    "das_plan_create_points": (_I, [ctypes.POINTER(_VP), _VP, _I, _VP, _F, _F, _F, _F, _I, _I, _I, _I, _I]),
     "das_plan_set_option": (_I, [_VP, _I, ctypes.c_double]),
     "das_plan_get_option": (_I, [_VP, _I, ctypes.POINTER(ctypes.c_double)]),
     "das_plan_kernel": (_I, [_VP, ctypes.POINTER(_I)]),
@@ -106,22 +107,33 @@ class Plan:
     """A DAS plan: fixed grid, receivers, physics constants, dtype and sizes."""
 
     def __init__(self, grid, rx_xyz, c, fs, t0=0.0, fnum=0.0, dtype="f32", B=1, Q=1, M=None,
-                 K=1, kernel="auto", f_demod=0.0, storage="native"):
+                 K=1, kernel="auto", f_demod=0.0, storage="native", points=None):
+        """``grid`` = (nx, ny, nz, x0, y0, z0, dx, dy, dz), or None with ``points``
+        an N x 3 array of voxel positions (das_plan_create_points)."""
         rx = np.ascontiguousarray(rx_xyz, dtype=np.float32).reshape(-1, 3)
         M = rx.shape[0] if M is None else M
         if M != rx.shape[0]:
             raise ValueError("M does not match rx_xyz")
-        self.grid = tuple(grid)
         self.dtype = dtype
         self.B, self.Q, self.M, self.K = int(B), int(Q), int(M), int(K)
-        self.N = self.grid[0] * self.grid[1] * self.grid[2]
-        g = _Grid(*[int(v) for v in self.grid[:3]], *[float(v) for v in self.grid[3:]])
         h = ctypes.c_void_p()
         dt = {"f32": DAS_F32, "c64": DAS_C64}[dtype]
         self._rx = rx
-        _check(lib().das_plan_create(ctypes.byref(h), ctypes.byref(g),
-                                     rx.ctypes.data_as(ctypes.c_void_p), c, fs, t0, fnum, dt,
-                                     self.B, self.Q, self.M, self.K))
+        if points is not None:
+            pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 3)
+            self.grid = None
+            self.N = pts.shape[0]
+            _check(lib().das_plan_create_points(
+                ctypes.byref(h), pts.ctypes.data_as(ctypes.c_void_p), self.N,
+                rx.ctypes.data_as(ctypes.c_void_p), c, fs, t0, fnum, dt, self.B, self.Q, self.M,
+                self.K))
+        else:
+            self.grid = tuple(grid)
+            self.N = self.grid[0] * self.grid[1] * self.grid[2]
+            g = _Grid(*[int(v) for v in self.grid[:3]], *[float(v) for v in self.grid[3:]])
+            _check(lib().das_plan_create(ctypes.byref(h), ctypes.byref(g),
+                                         rx.ctypes.data_as(ctypes.c_void_p), c, fs, t0, fnum, dt,
+                                         self.B, self.Q, self.M, self.K))
         self._h = h
         if kernel != "auto":
             self.set_option(OPT_KERNEL, KERNELS[kernel])
