@@ -123,19 +123,20 @@ class Oracle:
                  want_slack: bool = False, nthreads: int = 0):
         """Evaluates y[b, n] for the voxels ``idx`` (default: all of ``grid``).
 
-        ``rf`` is B x Q x M x K float32 or complex64; ``tau_tx``/``w_tx`` are
+        ``rf`` is B x Q x M x K float32, complex64, float64 or complex128;
+        ``tau_tx``/``w_tx`` are
         Q x N float32; ``rx_xyz`` is M x 3.  Voxel positions come from ``grid``
         (the regular-grid definition) unless ``vox_xyz`` (n_eval x 3) is given.
         Returns ``y`` (B x n_eval, float64 or complex128) and, with
         ``want_slack``, the per-output aperture-tie slack (B x n_eval).
         """
         rf = np.ascontiguousarray(rf)
-        if rf.dtype == np.complex64:
-            is_complex = 1
-        elif rf.dtype == np.float32:
-            is_complex = 0
-        else:
-            raise TypeError("rf must be float32 or complex64")
+        types = {np.dtype(np.float32): 0, np.dtype(np.complex64): 1,
+                 np.dtype(np.float64): 2, np.dtype(np.complex128): 3}
+        if rf.dtype not in types:
+            raise TypeError("rf must be float32, complex64, float64 or complex128")
+        rf_type = types[rf.dtype]
+        is_complex = rf_type & 1
         B, Q, M, K = rf.shape
         tau_tx = np.ascontiguousarray(tau_tx, dtype=np.float32)
         w_tx = np.ascontiguousarray(w_tx, dtype=np.float32)
@@ -155,7 +156,7 @@ class Oracle:
         out = np.zeros((B, n_eval, 2 if is_complex else 1), dtype=np.float64)
         slack = np.zeros((B, n_eval), dtype=np.float64) if want_slack else None
         rc = self._lib.das_oracle_beamform(
-            B, Q, M, K, N, rf.ctypes.data_as(ctypes.c_void_p), is_complex,
+            B, Q, M, K, N, rf.ctypes.data_as(ctypes.c_void_p), rf_type,
             _ptr(tau_tx, _F32P), _ptr(w_tx, _F32P), _ptr(rx, _F64P),
             _ptr(vox_xyz, _F64P), _ptr(idx, _I64P), n_eval,
             float(c), float(fs), float(t0), float(fnum), float(f_demod), float(tie_rel),

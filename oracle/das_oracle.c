@@ -78,21 +78,28 @@ int das_oracle_voxel_positions(int nx, int ny, int nz,
 }
 
 /* Sample k of receive line (b, q, m) in the B x Q x M x K record; zero outside
- * the record.  Complex data are interleaved (re, im) pairs. */
-static void sample_at(const float *rf, int is_complex, int Q, int M, int K,
+ * the record.  rf_type: 0 float32, 1 complex64, 2 float64, 3 complex128;
+ * complex data are interleaved (re, im) pairs. */
+static double element(const void *rf, int is_double, int64_t j)
+{
+    return is_double ? ((const double *)rf)[j] : (double)((const float *)rf)[j];
+}
+
+static void sample_at(const void *rf, int rf_type, int Q, int M, int K,
                       int b, int q, int m, int64_t k, double *re, double *im)
 {
+    const int is_double = rf_type >> 1;
     if (k < 0 || k > (int64_t)K - 1) {
         *re = 0.0;
         *im = 0.0;
         return;
     }
     const int64_t i = (((int64_t)b * Q + q) * M + m) * K + k;
-    if (is_complex) {
-        *re = (double)rf[2 * i];
-        *im = (double)rf[2 * i + 1];
+    if (rf_type & 1) {
+        *re = element(rf, is_double, 2 * i);
+        *im = element(rf, is_double, 2 * i + 1);
     } else {
-        *re = (double)rf[i];
+        *re = element(rf, is_double, i);
         *im = 0.0;
     }
 }
@@ -100,12 +107,12 @@ static void sample_at(const float *rf, int is_complex, int Q, int M, int K,
 /*
  * Evaluates y[:, n] for the n_eval voxels listed in vox_idx (positions in
  * vox_xyz, n_eval x 3).  tau_tx and w_tx are Q x N (float32, as the library
- * receives them); rf is B x Q x M x K (float32, or interleaved complex64 when
- * is_complex).  out is B x n_eval (x 2 interleaved when complex); slack is
- * B x n_eval or NULL.  Returns 0 on success.
+ * receives them); rf is B x Q x M x K of rf_type (0 float32, 1 complex64,
+ * 2 float64, 3 complex128; complex interleaved).  out is B x n_eval (x 2
+ * interleaved when complex); slack is B x n_eval or NULL.  Returns 0 on success.
  */
 int das_oracle_beamform(int B, int Q, int M, int K, int64_t N,
-                        const float *rf, int is_complex,
+                        const void *rf, int rf_type,
                         const float *tau_tx, const float *w_tx,
                         const double *rx_xyz,
                         const double *vox_xyz, const int64_t *vox_idx, int64_t n_eval,
@@ -113,6 +120,8 @@ int das_oracle_beamform(int B, int Q, int M, int K, int64_t N,
                         double tie_rel, double *out, double *slack, int nthreads)
 {
     if (B < 0 || Q < 0 || M < 0 || K < 0 || N < 0 || n_eval < 0) return ORACLE_EINVAL;
+    if (rf_type < 0 || rf_type > 3) return ORACLE_EINVAL;
+    const int is_complex = rf_type & 1;
     if (!(c > 0.0) || !(fs > 0.0)) return ORACLE_EINVAL;
     if (n_eval > 0 && (!vox_xyz || !vox_idx || !out)) return ORACLE_EINVAL;
     if ((int64_t)B * Q * M * K > 0 && !rf) return ORACLE_EINVAL;
@@ -173,8 +182,8 @@ int das_oracle_beamform(int B, int Q, int M, int K, int64_t N,
                 }
                 for (int b = 0; b < B; ++b) {
                     double s0r, s0i, s1r, s1i;
-                    sample_at(rf, is_complex, Q, M, K, b, q, m, k0, &s0r, &s0i);
-                    sample_at(rf, is_complex, Q, M, K, b, q, m, k0 + 1, &s1r, &s1i);
+                    sample_at(rf, rf_type, Q, M, K, b, q, m, k0, &s0r, &s0i);
+                    sample_at(rf, rf_type, Q, M, K, b, q, m, k0 + 1, &s1r, &s1i);
                     const double vr = (1.0 - a) * s0r + a * s1r;
                     const double vi = (1.0 - a) * s0i + a * s1i;
                     const double cr = wt * (vr * pr - vi * pim);

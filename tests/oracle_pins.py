@@ -206,6 +206,22 @@ def pin_bruteforce_complex(orc):
     assert np.abs(y - ref).max() <= 1e-12 * np.abs(ref).max(), np.abs(y - ref).max()
 
 
+def pin_bruteforce_float64_records(orc):
+    """float64 and complex128 records are read at full precision: values that
+    float32 cannot hold (1 + 1e-12 style) must survive into y."""
+    for seed, complex_data in ((17, False), (18, True)):
+        grid, rx, rf32, tau, w, c, fs = _small_random_case(seed, complex_data)
+        rng = np.random.default_rng(seed + 100)
+        rf = rf32.astype(np.complex128 if complex_data else np.float64)
+        rf = rf + rng.standard_normal(rf.shape) * 1e-9          # below float32 resolution
+        kw = dict(c=c, fs=fs, t0=0.5 / fs, fnum=1.0, f_demod=5e6 if complex_data else 0.0)
+        y = orc.beamform(rf, tau, w, rx, grid, **kw)
+        ref = das_bruteforce(rf, tau, w, rx, _grid_xyz(grid), **kw)
+        assert np.abs(y - ref).max() <= 1e-12 * np.abs(ref).max(), np.abs(y - ref).max()
+        y32 = orc.beamform(rf32, tau, w, rx, grid, **kw)
+        assert np.abs(y - y32).max() > 1e-12 * np.abs(ref).max()   # the perturbation is seen
+
+
 # --------------------------------------------------------------------------
 # invariants
 def pin_linearity(orc):
@@ -309,7 +325,8 @@ def pin_voxel_positions(orc):
 ALL_PINS = [
     pin_impulse_interior, pin_impulse_upper_edge, pin_impulse_lower_edge,
     pin_iq_constant_record, pin_all_ones_aperture_count, pin_aperture_tie_slack,
-    pin_bruteforce_real, pin_bruteforce_complex, pin_linearity, pin_shift_invariance,
+    pin_bruteforce_real, pin_bruteforce_complex, pin_bruteforce_float64_records,
+    pin_linearity, pin_shift_invariance,
     pin_point_scatterer_real, pin_point_scatterer_iq, pin_permute_matches_numpy,
     pin_voxel_positions,
 ]

@@ -25,8 +25,8 @@ MUTANTS = [
      "inside = (lhs <= rhs);"),
     ("receive delay units", "tau_t + dist / c", "tau_t + dist * c"),
     ("t0 sign", "(tau - t0) * fs", "(tau + t0) * fs"),
-    ("record axes q, m swapped", "const int64_t i = (((int64_t)b * Q + q) * M + m) * K + k;\n    if (is_complex)",
-     "const int64_t i = (((int64_t)b * M + m) * Q + q) * K + k;\n    if (is_complex)"),
+    ("record axes q, m swapped", "const int64_t i = (((int64_t)b * Q + q) * M + m) * K + k;\n    if (rf_type & 1)",
+     "const int64_t i = (((int64_t)b * M + m) * Q + q) * K + k;\n    if (rf_type & 1)"),
     ("permute reads q, m swapped", "const int64_t i = (((int64_t)b * Q + q) * M + m) * K + k;\n                    const int64_t o",
      "const int64_t i = (((int64_t)b * M + m) * Q + q) * K + k;\n                    const int64_t o"),
     ("last sample dropped", "if (k < 0 || k > (int64_t)K - 1) {",
@@ -39,6 +39,7 @@ MUTANTS = [
     ("slack signed", "slack[o] += sqrt(cr * cr + ci * ci);", "slack[o] += cr;"),
     ("permute q/m order", "(((int64_t)k * Q + q) * M + m) * B + b",
      "(((int64_t)k * M + m) * Q + q) * B + b"),
+    ("double records read as float", "const int is_double = rf_type >> 1;", "const int is_double = 0;"),
     ("grid y index", "const int64_t iy = (n / nx) % ny;", "const int64_t iy = (n / ny) % nx;"),
 ]
 
