@@ -57,7 +57,10 @@ typedef enum {
 /* Sample type of the RF record and of the output. */
 typedef enum {
     DAS_F32 = 0,   /* real float32 RF -> real float32 y */
-    DAS_C64 = 1    /* interleaved complex64 IQ -> complex64 y */
+    DAS_C64 = 1,   /* interleaved complex64 IQ -> complex64 y */
+    DAS_F64 = 2,   /* real float64 RF -> float64 y, computed in double; BL kernel only
+                      (ffdas docs, ALG1 supports float64 and complex128) */
+    DAS_C128 = 3   /* interleaved complex128 IQ -> complex128 y, in double; BL only */
 } das_dtype;
 
 /* Kernel choice (das_plan_set_option(DAS_OPT_KERNEL, ...)). */
@@ -121,7 +124,8 @@ typedef struct {
  *   c, fs    speed of sound (m/s) and sampling rate (Hz), both > 0.
  *   t0       time of sample 0 (seconds).
  *   fnum     receive F-number; <= 0 disables the aperture.
- *   dtype    DAS_F32 or DAS_C64.
+ *   dtype    DAS_F32, DAS_C64, DAS_F64 or DAS_C128 (the last two: BL kernel,
+ *            double-precision geometry and arithmetic; tau_tx and w_tx stay float32).
  *   B,Q,M,K  frames, transmits, receivers, samples per record (all >= 1);
  *            Q*M*(K+3) and B*N must stay below 2^31, K below 2^22.
  * Allocates the device copies of the geometry; the permute scratch of the BI

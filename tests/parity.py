@@ -9,9 +9,13 @@ import oracle as oracle_mod
 TOL = 1e-4   # max |y_gpu - y_oracle| (less the aperture-tie slack) / max |y_oracle|
 
 
+DTYPE_NAMES = {np.dtype(np.float32): "f32", np.dtype(np.complex64): "c64",
+               np.dtype(np.float64): "f64", np.dtype(np.complex128): "c128"}
+
+
 def plan_for(prob, kernel="auto"):
     from volumetric_ultrasound_delay_gb300 import das
-    dtype = "c64" if prob.rf.dtype == np.complex64 else "f32"
+    dtype = DTYPE_NAMES[prob.rf.dtype]
     return das.Plan(prob.grid, prob.rx, prob.c, prob.fs, prob.t0, prob.fnum, dtype,
                     prob.B, prob.Q, prob.M, prob.K, kernel=kernel, f_demod=prob.f_demod)
 

@@ -53,6 +53,7 @@ struct das_plan_s {
     cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
     RxPos *d_rx = nullptr;
     float4 *d_vox = nullptr;                  // voxel list (sample units), list plans only
+    Pos64 *d_rx64 = nullptr, *d_vox64 = nullptr;   // double copies, float64 / complex128 plans
     void *d_perm = nullptr;
     size_t perm_bytes = 0;
     bool perm_pads_zero = false;   // scratch holds the padded layout with zero pad rows
@@ -64,8 +65,11 @@ struct das_plan_s {
     cudaStream_t copy_stream = nullptr;
     std::vector<cudaEvent_t> copy_ev;         // [0]: start, [1]: tau/w copied, [2+g]: group g copied
     DasGeom geom{};
+    DasGeom64 geom64{};
 
-    size_t elem_bytes() const { return dtype == DAS_C64 ? 8 : 4; }
+    bool is_double() const { return dtype == DAS_F64 || dtype == DAS_C128; }
+    bool is_complex() const { return dtype == DAS_C64 || dtype == DAS_C128; }
+    size_t elem_bytes() const { return dtype == DAS_C128 ? 16 : (dtype == DAS_F32 ? 4 : 8); }
     size_t rf_bytes() const { return (size_t)B * Q * M * K * elem_bytes(); }
     size_t padded_bytes() const { return (size_t)B * Q * M * (K + 3) * elem_bytes(); }
     size_t out_bytes() const { return (size_t)B * (size_t)N * elem_bytes(); }
@@ -78,6 +82,7 @@ int resolve_kernel(const das_plan_s *p)
 {
     const bool cplx = p->dtype == DAS_C64;
     if (p->kernel != DAS_KERNEL_AUTO) return p->kernel;
+    if (p->is_double()) return DAS_KERNEL_BL;                     // the only double-precision kernel
     if (p->storage == DAS_STORAGE_F16) return DAS_KERNEL_BRICK;   // the only half-storage kernel
     if (das::brick_supported(p->B, cplx, p->K)) return DAS_KERNEL_BRICK;
     if (p->K >= 2 && das::bi_supported(p->B, cplx, p->bi_group)) return DAS_KERNEL_BI;
@@ -89,6 +94,8 @@ das_status check_supported(const das_plan_s *p, int kernel)
     const bool cplx = p->dtype == DAS_C64;
     if (p->storage == DAS_STORAGE_F16 && kernel != DAS_KERNEL_BRICK)
         return fail(DAS_ERR_UNSUPPORTED, "half-precision storage is served by the brick kernel only");
+    if (p->is_double() && kernel != DAS_KERNEL_BL)
+        return fail(DAS_ERR_UNSUPPORTED, "float64 / complex128 plans are served by the BL kernel only");
     switch (kernel) {
     case DAS_KERNEL_BL: return DAS_OK;
     case DAS_KERNEL_BI:
@@ -111,6 +118,8 @@ void release(das_plan_s *p)
 {
     cudaFree(p->d_rx);
     cudaFree(p->d_vox);
+    cudaFree(p->d_rx64);
+    cudaFree(p->d_vox64);
     cudaFree(p->d_perm);
     cudaFree(p->d_rf);
     cudaFree(p->d_out);
@@ -187,7 +196,7 @@ das_status das_plan_create(das_plan *plan, const das_grid *grid, const float *rx
     if (!(fs > 0.f) || !std::isfinite(fs)) return fail(DAS_ERR_INVALID_ARG, "fs must be > 0");
     if (!std::isfinite(t0) || !std::isfinite(fnum))
         return fail(DAS_ERR_INVALID_ARG, "t0 and fnum must be finite");
-    if (dtype != DAS_F32 && dtype != DAS_C64) return fail(DAS_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (dtype < DAS_F32 || dtype > DAS_C128) return fail(DAS_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
     if (B < 1 || Q < 1 || M < 1 || K < 1) return fail(DAS_ERR_INVALID_ARG, "B, Q, M, K must be >= 1");
     const long long N = (long long)grid->nx * grid->ny * grid->nz;
     if ((long long)Q * M * (K + 3) >= (1LL << 31))
@@ -228,8 +237,27 @@ das_status das_plan_create(das_plan *plan, const das_grid *grid, const float *rx
     g.rotate = 0;
     g.B = B; g.Q = Q; g.M = M; g.K = K;
 
+    DasGeom64 &g64 = p->geom64;
+    g64.nx = g.nx; g64.ny = g.ny; g64.nz = g.nz; g64.N = g.N;
+    g64.x0 = grid->x0 * s; g64.y0 = grid->y0 * s; g64.z0 = grid->z0 * s;
+    g64.dx = grid->dx * s; g64.dy = grid->dy * s; g64.dz = grid->dz * s;
+    g64.fs = fs;
+    g64.t0fs = (double)t0 * fs;
+    g64.aperture = g.aperture;
+    g64.ap2 = g.aperture ? 4.0 * (double)fnum * fnum : 0.0;
+    g64.fd_over_fs = 0.0;
+    g64.B = B; g64.Q = Q; g64.M = M; g64.K = K;
+    g64.vox = nullptr;
+
     e = cudaMalloc(&p->d_rx, sizeof(RxPos) * M);
     if (e == cudaSuccess) e = cudaMemcpy(p->d_rx, hrx.data(), sizeof(RxPos) * M, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && p->is_double()) {
+        std::vector<Pos64> h64(M);
+        for (int m = 0; m < M; ++m)
+            h64[m] = Pos64{rx_xyz[3 * m] * s, rx_xyz[3 * m + 1] * s, rx_xyz[3 * m + 2] * s, 0.0};
+        e = cudaMalloc(&p->d_rx64, sizeof(Pos64) * M);
+        if (e == cudaSuccess) e = cudaMemcpy(p->d_rx64, h64.data(), sizeof(Pos64) * M, cudaMemcpyHostToDevice);
+    }
     if (e != cudaSuccess) {
         release(p);
         delete p;
@@ -272,6 +300,21 @@ das_status das_plan_create_points(das_plan *plan, const float *voxel_xyz, int N,
         return cuda_fail(e, "voxel list upload");
     }
     p->geom.vox = p->d_vox;
+    if (p->is_double()) {
+        std::vector<Pos64> h64(N);
+        for (int n = 0; n < N; ++n)
+            h64[n] = Pos64{voxel_xyz[3 * n] * s, voxel_xyz[3 * n + 1] * s, voxel_xyz[3 * n + 2] * s, 0.0};
+        e = cudaMalloc(&p->d_vox64, sizeof(Pos64) * (size_t)N);
+        if (e == cudaSuccess)
+            e = cudaMemcpy(p->d_vox64, h64.data(), sizeof(Pos64) * (size_t)N, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) {
+            das_plan_destroy(p);
+            *plan = nullptr;
+            cudaGetLastError();
+            return cuda_fail(e, "voxel list upload");
+        }
+        p->geom64.vox = p->d_vox64;
+    }
     return DAS_OK;
 }
 
@@ -288,10 +331,11 @@ das_status das_plan_set_option(das_plan p, int option, double value)
     }
     case DAS_OPT_DEMOD_HZ:
         if (!std::isfinite(value)) return fail(DAS_ERR_INVALID_ARG, "f_demod must be finite");
-        if (p->dtype != DAS_C64 && value != 0.0)
-            return fail(DAS_ERR_UNSUPPORTED, "demodulation needs a DAS_C64 plan");
+        if (!p->is_complex() && value != 0.0)
+            return fail(DAS_ERR_UNSUPPORTED, "demodulation needs a complex (IQ) plan");
         p->f_demod = value;
         p->geom.fd_over_fs = (float)(value / (double)p->fs);
+        p->geom64.fd_over_fs = value / (double)p->fs;
         p->geom.rotate = value != 0.0;
         return DAS_OK;
     case DAS_OPT_TIMING:
@@ -366,7 +410,7 @@ das_status das_beamform(das_plan p, const void *rf, const float *tau_tx, const f
     das_status st = check_supported(p, kernel);
     if (st != DAS_OK) return st;
     DeviceGuard dg(p->device);
-    const bool cplx = p->dtype == DAS_C64;
+    const bool cplx = p->is_complex();
 
     const void *src = rf;
     const bool permute = kernel != DAS_KERNEL_BL;
@@ -386,7 +430,10 @@ das_status das_beamform(das_plan p, const void *rf, const float *tau_tx, const f
     if (e == cudaSuccess && p->timing) e = cudaEventRecord(p->ev[1], stream);
     if (e != cudaSuccess) return cuda_fail(e, "permute launch");
     switch (kernel) {
-    case DAS_KERNEL_BL: e = das::launch_bl(p->geom, p->d_rx, src, tau_tx, w_tx, out, cplx, stream); break;
+    case DAS_KERNEL_BL:
+        e = p->is_double() ? das::launch_bl64(p->geom64, p->d_rx64, src, tau_tx, w_tx, out, cplx, stream)
+                           : das::launch_bl(p->geom, p->d_rx, src, tau_tx, w_tx, out, cplx, stream);
+        break;
     case DAS_KERNEL_BI:
         e = das::launch_bi(p->geom, p->d_rx, src, tau_tx, w_tx, out, cplx, p->bi_group, stream);
         break;
@@ -503,6 +550,8 @@ das_status das_plan_device_bytes(das_plan p, size_t *bytes)
 {
     if (!p || !bytes) return fail(DAS_ERR_INVALID_ARG, "NULL argument");
     size_t b = sizeof(RxPos) * p->M + p->perm_bytes + (p->d_vox ? sizeof(float4) * (size_t)p->N : 0);
+    if (p->d_rx64) b += sizeof(Pos64) * p->M;
+    if (p->d_vox64) b += sizeof(Pos64) * (size_t)p->N;
     if (p->d_rf) b += p->rf_bytes();
     if (p->d_out) b += p->out_bytes();
     if (p->d_tau) b += p->txw_bytes();

@@ -27,6 +27,21 @@ struct DasGeom {
 // Receiver record of the plan: position in sample units.
 using RxPos = float4;
 
+// Double-precision geometry for float64 / complex128 plans (BL kernel only).
+struct Pos64 {
+    double x, y, z, pad;
+};
+struct DasGeom64 {
+    int nx, ny, nz;
+    int N;
+    double x0, y0, z0;    // first voxel, sample units
+    double dx, dy, dz;    // grid spacing, sample units
+    double fs, t0fs, ap2, fd_over_fs;
+    int aperture;
+    int B, Q, M, K;
+    const Pos64 *vox;     // voxel list (sample units), or nullptr for the grid
+};
+
 namespace das {
 
 // Sets the text das_last_error_string() returns on this thread.
@@ -40,6 +55,8 @@ cudaError_t launch_permute(const void *in, void *out, int elem_bytes, int B, int
                            bool to_half = false);
 cudaError_t launch_bl(const DasGeom &g, const RxPos *rx, const void *rf, const float *tau,
                       const float *w, void *out, bool cplx, cudaStream_t stream);
+cudaError_t launch_bl64(const DasGeom64 &g, const Pos64 *rx, const void *rf, const float *tau,
+                        const float *w, void *out, bool cplx, cudaStream_t stream);
 bool bi_supported(int B, bool cplx, int group);
 cudaError_t launch_bi(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
                       const float *w, void *out, bool cplx, int group, cudaStream_t stream);

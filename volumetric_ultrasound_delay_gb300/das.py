@@ -20,7 +20,8 @@ LIBRARY = Path(__file__).resolve().parent / "_lib" / "libdas.so"
 
 DAS_OK, DAS_ERR_INVALID_ARG, DAS_ERR_UNSUPPORTED, DAS_ERR_OUT_OF_MEMORY, DAS_ERR_CUDA, \
     DAS_ERR_TIMEOUT = range(6)
-DAS_F32, DAS_C64 = 0, 1
+DAS_F32, DAS_C64, DAS_F64, DAS_C128 = 0, 1, 2, 3
+_DTYPES = {"f32": DAS_F32, "c64": DAS_C64, "f64": DAS_F64, "c128": DAS_C128}
 KERNELS = {"auto": 0, "bl": 1, "bi": 2, "brick": 3}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 OPT_KERNEL, OPT_DEMOD_HZ, OPT_TIMING, OPT_BI_GROUP, OPT_HOST_GROUPS, OPT_STORAGE = 0, 1, 2, 3, 4, 5
@@ -117,7 +118,7 @@ class Plan:
         self.dtype = dtype
         self.B, self.Q, self.M, self.K = int(B), int(Q), int(M), int(K)
         h = ctypes.c_void_p()
-        dt = {"f32": DAS_F32, "c64": DAS_C64}[dtype]
+        dt = _DTYPES[dtype]
         self._rx = rx
         if points is not None:
             pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 3)
@@ -164,7 +165,8 @@ class Plan:
     # -- compute
     def _torch_dtypes(self):
         import torch
-        return torch.float32, (torch.complex64 if self.dtype == "c64" else torch.float32)
+        return torch.float32, {"f32": torch.float32, "c64": torch.complex64,
+                               "f64": torch.float64, "c128": torch.complex128}[self.dtype]
 
     def beamform(self, rf, tau_tx, w_tx, out=None, stream=None):
         """y (B x N) from device tensors rf (B x Q x M x K), tau_tx / w_tx (Q x N)."""
