@@ -52,7 +52,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="full", choices=["tiny", "mid", "full", "iq", "large"])
     ap.add_argument("--kernel", default="auto", choices=["auto", "bl", "bi", "brick"])
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -60,6 +60,8 @@ def parse_args():
     ap.add_argument("--n-el", type=int, default=None, help="override: array elements per side")
     ap.add_argument("--grid", type=int, nargs=3, default=None, metavar=("NX", "NY", "NZ"),
                     help="override: voxel grid (for small profiling cases)")
+    ap.add_argument("--storage", default="native", choices=["native", "f16"],
+                    help="element type of the permuted record copy (f16: half precision)")
     return ap.parse_args()
 
 
@@ -214,13 +216,13 @@ def source_sha(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def measured_traffic(kernel: str, workload: str):
+def measured_traffic(kernel: str, workload: str, storage: str = "native"):
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    key = f"{kernel}/{workload}"
+    key = f"{kernel}/{workload}" + ("" if storage == "native" else f"/{storage}")
     r = rec.get(key)
     if not r or r.get("source_sha") != source_sha(kernel):
         return None   # never measured, or the kernel changed since the counters were taken
@@ -284,7 +286,8 @@ def run_ours(args, world, rank, local):
     out = torch.empty((prob.B, prob.N), dtype=torch.complex64 if prob.wl.iq else torch.float32,
                       device=dev)
     plan = das.Plan(prob.grid, prob.rx, prob.c, prob.fs, prob.t0, prob.fnum, dtype, prob.B,
-                    prob.Q, prob.M, prob.K, kernel=args.kernel, f_demod=prob.f_demod)
+                    prob.Q, prob.M, prob.K, kernel=args.kernel, f_demod=prob.f_demod,
+                    storage=args.storage)
     kernel = plan.kernel
     plan.set_option(das.OPT_TIMING, 1)
     stream = torch.cuda.current_stream(dev)
@@ -324,14 +327,18 @@ def run_ours(args, world, rank, local):
         out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         plan.beamform_host(rf_h, tau_h, w_h, out_h, stream=stream)      # warm-up, allocates
         barrier(world)
-        t = time.perf_counter()
+        # median of the steps: the host link is shared with other jobs and an
+        # occasional step can take several times longer
+        e2e_t = []
         for _ in range(args.e2e_steps):
+            t = time.perf_counter()
             plan.beamform_host(rf_h, tau_h, w_h, out_h, stream=stream)
-        e2e_s = max_over_ranks(world, (time.perf_counter() - t) / args.e2e_steps)
+            e2e_t.append(time.perf_counter() - t)
+        e2e_s = max_over_ranks(world, statistics.median(e2e_t))
         e2e = {"value": world * A / e2e_s, "unit": UNIT,
                "h2d_bytes_per_step": int(rf_h.numel() * rf_h.element_size() + 2 * tau_h.numel() * 4),
                "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size()),
-               "ms_per_step": 1e3 * e2e_s}
+               "ms_per_step": 1e3 * e2e_s, "statistic": f"median of {args.e2e_steps} steps"}
         ref = out.cpu()
         if float((out_h - ref).abs().max()) > 1e-5 * float(ref.abs().max()):
             raise RuntimeError("host entry point disagrees with the device entry point")
@@ -351,7 +358,7 @@ def run_ours(args, world, rank, local):
     peak = props.multi_processor_count * FP32_LANES_PER_SM * sm_max * 1e6 / 1e12   # T issue/s
     das_mean = statistics.mean(das_ms)
     achieved = ISSUE_SLOTS_PER_ACC * a_eff / (das_mean / 1e3) / 1e12
-    traffic = measured_traffic(kernel, args.workload)
+    traffic = measured_traffic(kernel, args.workload, args.storage)
     roofline = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tinst/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "kernel": f"das_{kernel}_kernel", "kernel_ms": das_mean,
@@ -374,7 +381,7 @@ def run_ours(args, world, rank, local):
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "c64" if prob.wl.iq else "f32",
         "data": "synthetic (seeded numpy: N(0,1) noise + point-scatterer echoes)",
-        "config": {"workload": describe(prob.wl), "kernel": kernel,
+        "config": {"workload": describe(prob.wl), "kernel": kernel, "storage": args.storage,
                    "accumulations_per_step": A,
                    "in_aperture_fraction": pairs / (prob.N * prob.M),
                    "l2": f"inputs larger than L2 ({prob.rf.nbytes / 1e9:.2f} GB RF record), no flush",
