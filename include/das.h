@@ -72,10 +72,17 @@ typedef enum {
     DAS_KERNEL_BI = 2,     /* batch-inner warp tiling on a K x Q x M x B copy
                               (ffdas paper, Methods, batch-inner paragraphs /
                               Algorithm 2; ffdas docs, ALG2) */
-    DAS_KERNEL_BRICK = 3   /* this library's sm_103a design: voxel bricks per CTA,
+    DAS_KERNEL_BRICK = 3,  /* this library's sm_103a design: voxel bricks per CTA,
                               per-(voxel, transmit, receiver) geometry staged in
                               shared memory, receivers outside every aperture of
                               the brick skipped, zero-padded Q x M x (K+3) x B copy */
+    DAS_KERNEL_WINDOW = 4  /* this library's second sm_103a design on the same copy:
+                              a group of lanes owns a 2 x 2 quad of voxels and loads
+                              the window of rows the quad needs for a (transmit,
+                              receiver) once, with one coefficient per voxel and row.
+                              float32 records with B in {8, 16, 32} only; on request
+                              (AUTO keeps the brick kernel, faster on the workloads
+                              measured so far) */
 } das_kernel;
 
 /* Plan options. */
@@ -88,7 +95,7 @@ typedef enum {
                               das_plan_last_times); 0 (default): no events */
     DAS_OPT_BI_GROUP = 3,  /* BI kernel: lanes per voxel G in {2,4,8,16,32}; 0 = automatic */
     DAS_OPT_STORAGE = 5,   /* das_storage value: element type of the permuted copy */
-    DAS_OPT_HOST_GROUPS = 4 /* das_beamform_host with the brick kernel: number of transmit
+    DAS_OPT_HOST_GROUPS = 4 /* das_beamform_host with the brick or window kernel: number of transmit
                               groups the record is streamed in (copy of group g+1
                               overlapping the permute and sum of group g); 0 (default) =
                               min(Q, 5), 1 = copy everything first.  Summing in groups
@@ -128,8 +135,8 @@ typedef struct {
  *            double-precision geometry and arithmetic; tau_tx and w_tx stay float32).
  *   B,Q,M,K  frames, transmits, receivers, samples per record (all >= 1);
  *            Q*M*(K+3) and B*N must stay below 2^31, K below 2^22.
- * Allocates the device copies of the geometry; the permute scratch of the BI
- * and brick kernels (B*Q*M*(K+3) elements) is allocated on first use.
+ * Allocates the device copies of the geometry; the permute scratch of the BI,
+ * brick and window kernels (B*Q*M*(K+3) elements) is allocated on first use.
  * Errors: DAS_ERR_INVALID_ARG, DAS_ERR_OUT_OF_MEMORY, DAS_ERR_CUDA; *plan is
  * set to NULL on failure.  The plan belongs to the device current at creation.
  */
@@ -144,8 +151,9 @@ das_status das_plan_create(das_plan *plan, const das_grid *grid, const float *rx
  * tau_tx / w_tx arrays are indexed by list position n.
  *   voxel_xyz  host, N x 3 float32 positions (metres), copied.
  *   other arguments as das_plan_create.
- * The brick kernel takes bricks of consecutive list entries, so ordering the
- * list so that neighbours in it are neighbours in space keeps its caches warm.
+ * The brick and window kernels take bricks of consecutive list entries (the
+ * window kernel quads of four), so ordering the list so that neighbours in it
+ * are neighbours in space keeps their caches warm and the windows short.
  * Errors: as das_plan_create.
  */
 das_status das_plan_create_points(das_plan *plan, const float *voxel_xyz, int N,
@@ -168,7 +176,7 @@ das_status das_plan_kernel(das_plan plan, int *kernel);
  *   w_tx     device, Q x N float32 transmit weights.
  *   out      device, B x N (float32 or complex64); fully overwritten.
  *   stream   CUDA stream of the plan's device (0 = legacy default stream).
- * The BI and brick kernels first permute rf into the plan's scratch (ffdas
+ * The BI, brick and window kernels first permute rf into the plan's scratch (ffdas
  * paper, Methods, batch-inner paragraph; ffdas docs, ALG2: permuted as part of
  * the launch), so one plan must not run two das_beamform calls at once; use one
  * plan per concurrent stream.
@@ -182,7 +190,7 @@ das_status das_beamform(das_plan plan, const void *rf, const float *tau_tx,
 /*
  * The same computation from host buffers (same layouts as das_beamform, host
  * memory): copies the inputs to plan-owned device buffers, computes, copies y
- * back and synchronises `stream` before returning.  With the brick kernel the
+ * back and synchronises `stream` before returning.  With the brick or window kernel the
  * record is streamed in groups of transmits (DAS_OPT_HOST_GROUPS) on an internal
  * copy stream, so the copy of one group overlaps the permute and sum of the
  * previous one; the other kernels copy everything, then run das_beamform.

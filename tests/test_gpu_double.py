@@ -73,7 +73,7 @@ def test_double_host_path_and_rejections(oracle):
     plan.beamform_host(np.ascontiguousarray(prob.rf), prob.tau_tx, prob.w_tx, out)
     ref, slack = oracle_beamform(oracle, prob)
     assert error_ratio(out, ref, slack) <= TOL64
-    for kernel in ("bi", "brick"):
+    for kernel in ("bi", "brick", "window"):
         plan.kernel = kernel
         with pytest.raises(das.DasError) as exc:
             plan.beamform(*device_inputs(prob))

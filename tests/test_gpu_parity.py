@@ -20,7 +20,12 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():  # pragma: no cover - CPU containers skip these
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
-KERNELS = ["bl", "bi", "brick"]
+KERNELS = ["bl", "bi", "brick", "window"]
+
+
+def window_serves(prob):
+    """The window kernel takes float32 records of 8, 16 or 32 frames."""
+    return prob.rf.dtype == np.float32 and prob.B in (8, 16, 32)
 
 # Workloads shrunk (8x8 array, small ragged grids) so the oracle finishes in a
 # second or two; B, Q, K, dtype and transmit geometry are those of each workload.
@@ -80,7 +85,13 @@ def test_permute_bit_exact(oracle, shape, dtype, layout):
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("name", list(SMALL))
 def test_small_workload_all_voxels(oracle, small_problems, name, kernel):
+    from volumetric_ultrasound_delay_gb300 import das
     prob = small_problems[name]
+    if kernel == "window" and not window_serves(prob):
+        with pytest.raises(das.DasError) as exc:
+            gpu_beamform(prob, kernel)
+        assert exc.value.status == das.DAS_ERR_UNSUPPORTED
+        return
     y, used = gpu_beamform(prob, kernel)
     assert used == kernel
     ref, slack = oracle_beamform(oracle, prob)
@@ -88,15 +99,18 @@ def test_small_workload_all_voxels(oracle, small_problems, name, kernel):
     assert ratio <= TOL, (name, kernel, ratio)
 
 
-def test_auto_picks_brick_and_kernels_agree(small_problems):
-    prob = small_problems["full_s"]
-    outs = {k: gpu_beamform(prob, k)[0] for k in KERNELS}
+@pytest.mark.parametrize("name,auto", [("full_s", "brick"), ("large_s", "brick"),
+                                       ("iq_s", "brick")])
+def test_auto_choice_and_kernels_agree(small_problems, name, auto):
+    prob = small_problems[name]
+    kernels = [k for k in KERNELS if k != "window" or window_serves(prob)]
+    outs = {k: gpu_beamform(prob, k)[0] for k in kernels}
     y_auto, used = gpu_beamform(prob, "auto")
-    assert used == "brick"
-    assert np.array_equal(y_auto, outs["brick"])
+    assert used == auto
+    assert np.array_equal(y_auto, outs[auto])
     peak = np.abs(outs["bl"]).max()
-    for k in ("bi", "brick"):
-        assert np.abs(outs[k] - outs["bl"]).max() <= TOL * peak
+    for k in kernels:
+        assert np.abs(outs[k] - outs["bl"]).max() <= TOL * peak, k
 
 
 # ------------------------------------------------------------- edge cases
@@ -125,6 +139,10 @@ EDGE = {
     "iq_B32": dict(iq=True, fs=10e6, f_demod=5e6, B=32, K=128),
     "f32_B64": dict(B=64, K=96),
     "f32_B128": dict(B=128, K=64),
+    "B16": dict(B=16),
+    "B32": dict(B=32, K=96),
+    # neighbouring voxels many samples apart: windows too wide, two rows per voxel
+    "coarse_grid": dict(B=32, half_width=15e-3, K=1024, fnum=0.0),
 }
 
 
@@ -137,7 +155,9 @@ def test_edge_cases(oracle, name):
         try:
             y, _ = gpu_beamform(prob, kernel)
         except das.DasError as exc:
-            assert exc.status == das.DAS_ERR_UNSUPPORTED and kernel in ("bi", "brick"), (name, kernel)
+            assert exc.status == das.DAS_ERR_UNSUPPORTED and kernel in ("bi", "brick", "window"), \
+                (name, kernel)
+            assert kernel != "window" or not window_serves(prob), name
             continue
         assert error_ratio(y, ref, slack) <= TOL, (name, kernel, error_ratio(y, ref, slack))
 
@@ -164,7 +184,7 @@ def test_all_outside_aperture_is_zero():
 def test_unsupported_requests_are_rejected():
     from volumetric_ultrasound_delay_gb300 import das
     prob = _custom(B=3)
-    for kernel in ("bi", "brick"):
+    for kernel in ("bi", "brick", "window"):
         with pytest.raises(das.DasError) as exc:
             gpu_beamform(prob, kernel)
         assert exc.value.status == das.DAS_ERR_UNSUPPORTED
@@ -192,16 +212,17 @@ def test_misaligned_and_wrong_sizes_rejected():
 
 
 @pytest.mark.parametrize("groups", [1, 0, 4, 9])
-@pytest.mark.parametrize("name", ["full_s", "iq_s", "large_s"])
-def test_host_entry_point_matches_device(oracle, small_problems, name, groups):
+@pytest.mark.parametrize("name,kernel", [("full_s", "auto"), ("iq_s", "auto"), ("large_s", "auto"),
+                                         ("full_s", "window"), ("large_s", "window")])
+def test_host_entry_point_matches_device(oracle, small_problems, name, kernel, groups):
     """Host buffers in, host buffer out: copying everything first (groups=1)
     reproduces the device entry point bit for bit; streaming the record in
     transmit groups (0 = automatic, 4 = uneven groups of 2-3 transmits, 9 = one
     per transmit) only changes the float32 summation order."""
     from volumetric_ultrasound_delay_gb300 import das
     prob = small_problems[name]
-    y_dev, _ = gpu_beamform(prob)
-    plan = plan_for(prob)
+    y_dev, _ = gpu_beamform(prob, kernel)
+    plan = plan_for(prob, kernel)
     plan.set_option(das.OPT_HOST_GROUPS, groups)
     out = torch.empty((prob.B, prob.N), dtype=torch.complex64 if prob.wl.iq else torch.float32).pin_memory()
     rf = torch.from_numpy(np.ascontiguousarray(prob.rf)).pin_memory()
@@ -247,7 +268,8 @@ def test_full_size_sampled(oracle, name, samples):
     inputs = device_inputs(prob)
     idx = synth.sample_voxels(prob.N, samples, seed=prob.wl.seed)
     ref, slack = oracle_beamform(oracle, prob, idx=idx)
-    kernels = ["auto", "bi"] + (["bl"] if name in ("mid", "full") else [])
+    kernels = ["auto", "bi"] + (["window"] if name != "iq" else []) + \
+        (["bl"] if name in ("mid", "full") else [])
     for kernel in kernels:
         y, used = gpu_beamform(prob, kernel, inputs=inputs)
         ratio = error_ratio(y[:, idx], ref, slack)

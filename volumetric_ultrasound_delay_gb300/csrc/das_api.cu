@@ -110,6 +110,13 @@ das_status check_supported(const das_plan_s *p, int kernel)
                         "brick kernel needs K >= 2 and B * element size in {32, 64, 128, 256, 512} "
                         "bytes (half storage: {16, ..., 64, 128, 256}) (B=%d)", p->B);
         return DAS_OK;
+    case DAS_KERNEL_WINDOW:
+        if (!das::window_supported(p->B, cplx, p->K, p->Q, p->M))
+            return fail(DAS_ERR_UNSUPPORTED,
+                        "window kernel needs a float32 record with B in {8, 16, 32}, K >= 2, "
+                        "Q x M x (K+3) < 2^31 and its transmit table in shared memory "
+                        "(B=%d, Q=%d)", p->B, p->Q);
+        return DAS_OK;
     default: return fail(DAS_ERR_INVALID_ARG, "unknown kernel %d", kernel);
     }
 }
@@ -324,7 +331,7 @@ das_status das_plan_set_option(das_plan p, int option, double value)
     switch (option) {
     case DAS_OPT_KERNEL: {
         const int k = (int)value;
-        if ((double)k != value || k < DAS_KERNEL_AUTO || k > DAS_KERNEL_BRICK)
+        if ((double)k != value || k < DAS_KERNEL_AUTO || k > DAS_KERNEL_WINDOW)
             return fail(DAS_ERR_INVALID_ARG, "invalid kernel %g", value);
         p->kernel = k;
         return DAS_OK;
@@ -437,6 +444,9 @@ das_status das_beamform(das_plan p, const void *rf, const float *tau_tx, const f
     case DAS_KERNEL_BI:
         e = das::launch_bi(p->geom, p->d_rx, src, tau_tx, w_tx, out, cplx, p->bi_group, stream);
         break;
+    case DAS_KERNEL_WINDOW:
+        e = das::launch_window(p->geom, p->d_rx, src, tau_tx, w_tx, out, stream);
+        break;
     default:
         e = das::launch_brick(p->geom, p->d_rx, src, tau_tx, w_tx, out, cplx, stream, 0, -1, false, half);
         break;
@@ -470,7 +480,8 @@ das_status das_beamform_host(das_plan p, const void *rf_host, const float *tau_t
         return cuda_fail(e, "host-path device buffers");
     }
     int groups = p->host_groups > 0 ? p->host_groups : (p->Q < 5 ? p->Q : 5);
-    if (kernel != DAS_KERNEL_BRICK) groups = 1;     // only the brick kernel sums transmit ranges
+    if (kernel != DAS_KERNEL_BRICK && kernel != DAS_KERNEL_WINDOW)
+        groups = 1;                                  // only these kernels sum transmit ranges
     if (groups > p->Q) groups = p->Q;
 
     if (groups <= 1) {
@@ -522,8 +533,11 @@ das_status das_beamform_host(das_plan p, const void *rf_host, const float *tau_t
                 e = das::launch_permute(p->d_rf, p->d_perm, (int)eb, p->B, p->Q, p->M, p->K, 2,
                                         p->num_sms, stream, q0, q1, half);
             if (e == cudaSuccess)
-                e = das::launch_brick(p->geom, p->d_rx, p->d_perm, p->d_tau, p->d_w, p->d_out, cplx,
-                                      stream, q0, q1, gi > 0, half);
+                e = kernel == DAS_KERNEL_WINDOW
+                        ? das::launch_window(p->geom, p->d_rx, p->d_perm, p->d_tau, p->d_w, p->d_out,
+                                             stream, q0, q1, gi > 0)
+                        : das::launch_brick(p->geom, p->d_rx, p->d_perm, p->d_tau, p->d_w, p->d_out,
+                                            cplx, stream, q0, q1, gi > 0, half);
         }
         if (e != cudaSuccess) return cuda_fail(e, "streamed beamform launch");
     }

@@ -66,5 +66,10 @@ bool brick_supported(int B, bool cplx, int K, bool half = false);
 cudaError_t launch_brick(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
                          const float *w, void *out, bool cplx, cudaStream_t stream, int q0 = 0,
                          int q1 = -1, bool accumulate = false, bool half = false);
+bool window_supported(int B, bool cplx, int K, int Q, int M, bool half = false);
+// float32 records only; transmits [q0, q1), accumulate as for the brick kernel
+cudaError_t launch_window(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
+                          const float *w, void *out, cudaStream_t stream, int q0 = 0, int q1 = -1,
+                          bool accumulate = false);
 
 }  // namespace das
