@@ -13,7 +13,7 @@
 // lanes owns one voxel and reads the voxel's two rows in 16-byte chunks:
 //   pair mode  : lane t loads chunks t, t + G, ... of both rows (float32 data,
 //                and half-precision rows of more than 64 bytes); G = 8 lanes
-//                cover one 128-byte line per row;
+//                cover one 128-byte line per row (16 lanes two lines);
 //   split mode : half-precision rows of at most 64 bytes: the 2 * CPR chunks of
 //                the two adjacent rows go one per lane (G = 2 * CPR), so a group
 //                reads one contiguous run; the partial sums of the two rows are
@@ -194,11 +194,14 @@ __device__ __forceinline__ void accumulate(float2 (&acc)[NA][NP], float wq, floa
 }
 
 // CTAs per SM the register allocation must allow: lanes that hold more chunks
-// (J) or complex samples keep more row data in flight per trip
-template <int J, bool CPLX, bool HALF>
+// (J) or complex samples keep more row data in flight per trip; 16-lane groups
+// (at most two chunks a lane) fit 4 CTAs per SM, 3 for complex with 4 entries
+// per trip
+template <int G, int J, bool CPLX, bool HALF>
 constexpr int min_blocks()
 {
-    return J >= 4 ? 2 : (J == 2 || CPLX ? 3 : (HALF ? 5 : DAS_BRICK_MIN_BLOCKS));
+    return G == 16 ? (CPLX && J == 1 ? 3 : 4)
+                   : (J >= 4 ? 2 : (J == 2 || CPLX ? 3 : (HALF ? 5 : DAS_BRICK_MIN_BLOCKS)));
 }
 
 // receivers per phase-C trip
@@ -206,7 +209,7 @@ template <int J, bool HALF>
 constexpr int trip_size() { return J >= 4 ? 1 : (J == 2 ? 2 : (HALF ? 2 : DAS_BRICK_U1)); }
 
 template <int G, int J, bool CPLX, bool HALF, bool SPLIT>
-__global__ void __launch_bounds__(THREADS, min_blocks<J, CPLX, HALF>())
+__global__ void __launch_bounds__(THREADS, min_blocks<G, J, CPLX, HALF>())
 das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict__ perm,
                  const float *__restrict__ tau, const float *__restrict__ wtx,
                  float *__restrict__ out, int bricks_x, int bricks_y, int fb, int q_begin,
@@ -490,7 +493,9 @@ cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, cons
 
 // Lanes per voxel G, chunks J, and split mode for B frames.
 //   float32 / complex64 storage: pair mode, CPR = B * size / 16 chunks per row,
-//     G = CPR if <= 8 (J = 1), else G = 8 and J = CPR / 8 in {2, 4};
+//     G = CPR if <= 8 (J = 1); rows of 16 or 32 chunks G = 16, J = CPR / 16
+//     (16 lanes at one or two chunks each leave room for 4 CTAs per SM, where
+//     8 lanes at four chunks fit only 2); else G = 8, J = CPR / 8 in {2, 4};
 //   half / half2 storage: rows of <= 64 bytes (CPR <= 4) use split mode with
 //     G = 2 CPR; wider rows pair mode with G = 8, J = CPR / 8 in {1, 2}.
 bool choose(int B, bool cplx, bool half, int &G, int &J, bool &split)
@@ -514,6 +519,11 @@ bool choose(int B, bool cplx, bool half, int &G, int &J, bool &split)
         G = cpr;
         J = 1;
         return G == 2 || G == 4 || G == 8;
+    }
+    if (cpr == 16 || cpr == 32) {
+        G = 16;         // rows of 256 or 512 bytes: 16 lanes, one or two chunks each
+        J = cpr / 16;
+        return true;
     }
     G = 8;
     J = cpr / 8;
@@ -545,6 +555,7 @@ cudaError_t launch_brick(const DasGeom &g, const RxPos *rx, const void *perm, co
     DAS_BRICK_CASE(2, 1, false, false) DAS_BRICK_CASE(4, 1, false, false)
     DAS_BRICK_CASE(8, 1, false, false) DAS_BRICK_CASE(8, 2, false, false)
     DAS_BRICK_CASE(8, 4, false, false)
+    DAS_BRICK_CASE(16, 1, false, false) DAS_BRICK_CASE(16, 2, false, false)
     DAS_BRICK_CASE(2, 1, true, true) DAS_BRICK_CASE(4, 1, true, true) DAS_BRICK_CASE(8, 1, true, true)
     DAS_BRICK_CASE(8, 1, true, false) DAS_BRICK_CASE(8, 2, true, false)
 #undef DAS_BRICK_CASE
