@@ -80,11 +80,6 @@ __device__ __forceinline__ float2 demod_phase(const DasGeom &g, float f)
     return make_float2(c, s);
 }
 
-__device__ __forceinline__ float2 cmul(float2 a, float2 b)
-{
-    return make_float2(a.x * b.x - a.y * b.y, a.x * b.y + a.y * b.x);
-}
-
 // acc += w * s for complex w, s (4 FMA)
 __device__ __forceinline__ void cfma(float2 &acc, float2 w, float2 s)
 {
