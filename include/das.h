@@ -234,6 +234,17 @@ das_status das_permute(const void *in, void *out, das_dtype dtype, int B, int Q,
                        int K, int layout, das_storage storage, cudaStream_t stream);
 
 /*
+ * The batch-inner permute by itself: B x Q x M x K -> K x Q x M x B, bit for
+ * bit (ffdas paper, Methods, batch-inner paragraph; ffdas docs, ALG2, the
+ * permute done as part of the launch).  Same as das_permute with layout 0 and
+ * DAS_STORAGE_NATIVE: dtype DAS_F32 or DAS_C64, in and out device buffers of
+ * B*Q*M*K elements that must not overlap.
+ * Errors: DAS_ERR_INVALID_ARG, DAS_ERR_CUDA.  Asynchronous.
+ */
+das_status das_permute_bqmk_to_kqmb(const void *in, void *out, das_dtype dtype, int B, int Q,
+                                    int M, int K, cudaStream_t stream);
+
+/*
  * das_beamform_noalloc -- the same computation as a plan running the brick
  * kernel, for callers that cannot allocate device memory.  The ffdas pages
  * have no counterpart to this entry point.

@@ -65,4 +65,7 @@ def test_host_side_rejections(libdas):
     assert libdas.das_permute(buf, buf, 0, 1, 1, 1, 4, 0, 0, None) == das.DAS_ERR_INVALID_ARG  # overlap
     assert libdas.das_permute(buf, ctypes.byref(buf, 32), 0, 1, 1, 1, 4, 3, 0, None) == das.DAS_ERR_INVALID_ARG  # bad layout
     assert libdas.das_permute(buf, ctypes.byref(buf, 32), 0, 1, 1, 1, 4, 0, 7, None) == das.DAS_ERR_INVALID_ARG  # bad storage
+    assert libdas.das_permute_bqmk_to_kqmb(None, None, 0, 1, 1, 1, 1, None) == das.DAS_ERR_INVALID_ARG
+    assert libdas.das_permute_bqmk_to_kqmb(buf, buf, 0, 1, 1, 1, 4, None) == das.DAS_ERR_INVALID_ARG  # overlap
+    assert libdas.das_permute_bqmk_to_kqmb(buf, ctypes.byref(buf, 32), 5, 1, 1, 1, 4, None) == das.DAS_ERR_INVALID_ARG
     assert libdas.das_version() == b"1.0.0"

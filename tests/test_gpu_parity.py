@@ -81,6 +81,23 @@ def test_permute_bit_exact(oracle, shape, dtype, layout):
     assert dst.cpu().numpy().tobytes() == want.tobytes()
 
 
+@pytest.mark.parametrize("dtype", ["f32", "c64"])
+def test_batch_inner_permute_entry_point(oracle, dtype):
+    """das_permute_bqmk_to_kqmb: the pages' K x Q x M x B layout, bit for bit."""
+    from volumetric_ultrasound_delay_gb300 import das
+    rng = np.random.default_rng(31)
+    shape = (24, 3, 7, 130)
+    if dtype == "c64":
+        x = (rng.standard_normal(shape) + 1j * rng.standard_normal(shape)).astype(np.complex64)
+    else:
+        x = rng.standard_normal(shape).astype(np.float32)
+    src = torch.from_numpy(x).cuda()
+    dst = torch.empty_like(src).reshape(-1)
+    das.permute_bqmk_to_kqmb(src, dst)
+    torch.cuda.synchronize()
+    assert dst.cpu().numpy().tobytes() == oracle.permute(x, "kqmb").tobytes()
+
+
 # ------------------------------------------------- small workloads, all voxels
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("name", list(SMALL))

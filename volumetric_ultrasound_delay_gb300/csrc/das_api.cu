@@ -612,4 +612,10 @@ das_status das_permute(const void *in, void *out, das_dtype dtype, int B, int Q,
     return DAS_OK;
 }
 
+das_status das_permute_bqmk_to_kqmb(const void *in, void *out, das_dtype dtype, int B, int Q, int M,
+                                    int K, cudaStream_t stream)
+{
+    return das_permute(in, out, dtype, B, Q, M, K, 0, DAS_STORAGE_NATIVE, stream);
+}
+
 }  // extern "C"

@@ -43,6 +43,7 @@ _SIGS = {
     "das_plan_device_bytes": (_I, [_VP, ctypes.POINTER(ctypes.c_size_t)]),
     "das_plan_destroy": (_I, [_VP]),
     "das_permute": (_I, [_VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP]),
+    "das_permute_bqmk_to_kqmb": (_I, [_VP, _VP, _I, _I, _I, _I, _I, _VP]),
     "das_beamform_noalloc": (_I, [_VP, _VP, _F, _F, _F, _F, ctypes.c_double, _I, _I, _I, _I, _I,
                                   _VP, _VP, _VP, _VP, _VP]),
     "das_last_error_string": (ctypes.c_char_p, []),
@@ -246,6 +247,18 @@ def permute(rf, out, layout: int = 0, stream=None, storage: str = "native"):
     st = {"native": STORAGE_NATIVE, "f16": STORAGE_F16}[storage]
     _check(lib().das_permute(_dev_ptr(rf, "rf"), optr, dt, B, Q, M, K, layout, st,
                              _stream_handle(stream)))
+    return out
+
+
+def permute_bqmk_to_kqmb(rf, out, stream=None):
+    """das_permute_bqmk_to_kqmb: B x Q x M x K -> K x Q x M x B, bit for bit."""
+    import torch
+    if rf.dtype not in (torch.float32, torch.complex64) or rf.dim() != 4:
+        raise TypeError("rf must be a 4-D float32 or complex64 CUDA tensor")
+    B, Q, M, K = rf.shape
+    dt = DAS_C64 if rf.dtype == torch.complex64 else DAS_F32
+    _check(lib().das_permute_bqmk_to_kqmb(_dev_ptr(rf, "rf"), _dev_ptr(out, "out", rf.dtype, B * Q * M * K),
+                                          dt, B, Q, M, K, _stream_handle(stream)))
     return out
 
 
