@@ -116,17 +116,23 @@ typedef enum {
 } das_storage;
 
 /* Regular voxel grid: voxel n = ix + nx*(iy + ny*iz) sits at
- * (x0 + ix*dx, y0 + iy*dy, z0 + iz*dz), metres.  The receivers face +z. */
+ * (x0 + ix*dx, y0 + iy*dy, z0 + iz*dz), metres.  The receivers face +z.
+ * xyz (optional, may be NULL): host N x 3 float32 positions (metres) of the
+ * N = nx*ny*nz voxels in the order n; when given, das_plan_create builds a
+ * voxel-list plan (as das_plan_create_points) and origin and spacing are
+ * ignored. */
 typedef struct {
     int nx, ny, nz;
     float x0, y0, z0;
     float dx, dy, dz;
+    const float *xyz;
 } das_grid;
 
 /*
  * Creates a plan for fixed geometry and sizes (ffdas paper, Methods: geometry
  * on the fly; the call follows the problem statement of the method).
- *   grid     host, regular voxel grid (N = nx*ny*nz voxels), copied.
+ *   grid     host, regular voxel grid (N = nx*ny*nz voxels), copied; with
+ *            grid->xyz set, the explicit voxel list of das_plan_create_points.
  *   rx_xyz   host, M x 3 float32 receiver positions (metres), copied.
  *   c, fs    speed of sound (m/s) and sampling rate (Hz), both > 0.
  *   t0       time of sample 0 (seconds).

@@ -55,6 +55,11 @@ def test_host_side_rejections(libdas):
     assert b"K must be" in libdas.das_last_error_string()
     bad = das._Grid(0, 4, 4, 0.0, 0.0, 0.01, 1e-3, 1e-3, 1e-3)
     assert libdas.das_plan_create(ctypes.byref(h), ctypes.byref(bad), rx, 1540.0, 20e6, 0.0, 1.5, 0, 1, 1, 1, 8) == das.DAS_ERR_INVALID_ARG
+    # a grid carrying a voxel list goes through the list checks (a NaN position)
+    pts = (ctypes.c_float * (3 * 64))(*([0.0] * (3 * 64 - 1) + [float("nan")]))
+    listed = das._Grid(4, 4, 4, 0.0, 0.0, 0.01, 1e-3, 1e-3, 1e-3, ctypes.cast(pts, ctypes.c_void_p))
+    assert libdas.das_plan_create(ctypes.byref(h), ctypes.byref(listed), rx, 1540.0, 20e6, 0.0, 1.5, 0, 1, 1, 1, 8) == das.DAS_ERR_INVALID_ARG
+    assert b"voxel position" in libdas.das_last_error_string()
     # calls on a NULL plan
     assert libdas.das_beamform(None, None, None, None, None, None) == das.DAS_ERR_INVALID_ARG
     assert libdas.das_plan_set_option(None, 0, 0.0) == das.DAS_ERR_INVALID_ARG

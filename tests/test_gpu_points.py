@@ -56,6 +56,29 @@ def test_sampled_grid_voxels_as_a_list(oracle, base, kernel):
     assert np.abs(y - y_grid[:, idx]).max() <= TOL * np.abs(y_grid).max()
 
 
+def test_list_through_the_grid_struct_matches_points_plan():
+    """das_plan_create with grid.xyz set builds the same plan as
+    das_plan_create_points: identical output, bit for bit."""
+    from volumetric_ultrasound_delay_gb300 import das
+    prob = synth.make_problem("full", n_el=8, nx=19, ny=13, nz=5)
+    rng = np.random.default_rng(23)
+    idx = rng.choice(prob.N, 240, replace=False)
+    pts = synth.grid_points(prob.grid, idx).astype(np.float32)
+    tau, w = prob.tau_tx[:, idx], prob.w_tx[:, idx]
+    ys = []
+    for grid in (None, (4, 6, 10, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0)):
+        plan = das.Plan(grid, prob.rx, prob.c, prob.fs, prob.t0, prob.fnum, "f32", prob.B, prob.Q,
+                        prob.M, prob.K, points=pts)
+        assert plan.N == len(pts)
+        y = plan.beamform(torch.from_numpy(np.ascontiguousarray(prob.rf)).cuda(),
+                          torch.from_numpy(np.ascontiguousarray(tau)).cuda(),
+                          torch.from_numpy(np.ascontiguousarray(w)).cuda())
+        torch.cuda.synchronize()
+        ys.append(y.cpu().numpy())
+        plan.close()
+    assert np.array_equal(ys[0], ys[1])
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_random_point_cloud(oracle, kernel):
     prob = synth.make_problem("mid", n_el=8, nx=4, ny=4, nz=4, B=16)

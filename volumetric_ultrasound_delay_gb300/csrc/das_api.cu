@@ -196,6 +196,12 @@ das_status das_plan_create(das_plan *plan, const das_grid *grid, const float *rx
     if (!rx_xyz) return fail(DAS_ERR_INVALID_ARG, "rx_xyz is NULL");
     if (grid->nx < 1 || grid->ny < 1 || grid->nz < 1)
         return fail(DAS_ERR_INVALID_ARG, "grid dimensions must be >= 1");
+    if (grid->xyz) {
+        const long long n = (long long)grid->nx * grid->ny * grid->nz;
+        if (n >= (1LL << 31)) return fail(DAS_ERR_INVALID_ARG, "nx*ny*nz must be < 2^31");
+        return das_plan_create_points(plan, grid->xyz, (int)n, rx_xyz, c, fs, t0, fnum, dtype, B, Q,
+                                      M, K);
+    }
     const float gf[6] = {grid->x0, grid->y0, grid->z0, grid->dx, grid->dy, grid->dz};
     for (float v : gf)
         if (!std::isfinite(v)) return fail(DAS_ERR_INVALID_ARG, "grid origin/spacing not finite");
@@ -217,6 +223,7 @@ das_status das_plan_create(das_plan *plan, const das_grid *grid, const float *rx
     das_plan_s *p = new (std::nothrow) das_plan_s;
     if (!p) return fail(DAS_ERR_OUT_OF_MEMORY, "host allocation of the plan failed");
     p->grid = *grid;
+    p->grid.xyz = nullptr;   // the caller's list is copied below, not kept
     p->c = c; p->fs = fs; p->t0 = t0; p->fnum = fnum;
     p->dtype = dtype;
     p->B = B; p->Q = Q; p->M = M; p->K = K;
@@ -288,7 +295,7 @@ das_status das_plan_create_points(das_plan *plan, const float *voxel_xyz, int N,
     for (long long i = 0; i < 3LL * N; ++i)
         if (!std::isfinite(voxel_xyz[i])) return fail(DAS_ERR_INVALID_ARG, "voxel position not finite");
     // a 1 x 1 x N grid carries the sizes; the positions come from the list
-    const das_grid grid = {1, 1, N, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const das_grid grid = {1, 1, N, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, nullptr};
     das_status st = das_plan_create(plan, &grid, rx_xyz, c, fs, t0, fnum, dtype, B, Q, M, K);
     if (st != DAS_OK) return st;
     das_plan_s *p = *plan;

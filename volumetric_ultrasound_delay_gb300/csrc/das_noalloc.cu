@@ -62,6 +62,8 @@ extern "C" das_status das_beamform_noalloc(const das_grid *grid, const float *rx
         return reject(DAS_ERR_INVALID_ARG, "NULL argument");
     if (grid->nx < 1 || grid->ny < 1 || grid->nz < 1 || B < 1 || Q < 1 || M < 1 || K < 1)
         return reject(DAS_ERR_INVALID_ARG, "grid dimensions and B, Q, M, K must be >= 1");
+    if (grid->xyz)
+        return reject(DAS_ERR_UNSUPPORTED, "voxel lists need a plan (das_plan_create)");
     if (!(c > 0.f) || !(fs > 0.f) || !std::isfinite(c) || !std::isfinite(fs) ||
         !std::isfinite(t0) || !std::isfinite(fnum) || !std::isfinite(f_demod))
         return reject(DAS_ERR_INVALID_ARG, "c and fs must be > 0; t0, fnum, f_demod finite");

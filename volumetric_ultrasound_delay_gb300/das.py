@@ -59,7 +59,8 @@ class DasError(RuntimeError):
 
 class _Grid(ctypes.Structure):
     _fields_ = [("nx", _I), ("ny", _I), ("nz", _I),
-                ("x0", _F), ("y0", _F), ("z0", _F), ("dx", _F), ("dy", _F), ("dz", _F)]
+                ("x0", _F), ("y0", _F), ("z0", _F), ("dx", _F), ("dy", _F), ("dz", _F),
+                ("xyz", ctypes.c_void_p)]
 
 
 _LIB = None
@@ -111,7 +112,9 @@ class Plan:
     def __init__(self, grid, rx_xyz, c, fs, t0=0.0, fnum=0.0, dtype="f32", B=1, Q=1, M=None,
                  K=1, kernel="auto", f_demod=0.0, storage="native", points=None):
         """``grid`` = (nx, ny, nz, x0, y0, z0, dx, dy, dz), or None with ``points``
-        an N x 3 array of voxel positions (das_plan_create_points)."""
+        an N x 3 array of voxel positions (das_plan_create_points).  With both,
+        ``points`` (nx*ny*nz x 3) goes in the grid's voxel list (das_plan_create
+        with grid.xyz)."""
         rx = np.ascontiguousarray(rx_xyz, dtype=np.float32).reshape(-1, 3)
         M = rx.shape[0] if M is None else M
         if M != rx.shape[0]:
@@ -121,7 +124,18 @@ class Plan:
         h = ctypes.c_void_p()
         dt = _DTYPES[dtype]
         self._rx = rx
-        if points is not None:
+        if points is not None and grid is not None:
+            pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 3)
+            self.grid = None
+            self.N = int(grid[0]) * int(grid[1]) * int(grid[2])
+            if pts.shape[0] != self.N:
+                raise ValueError("points must hold nx*ny*nz positions")
+            g = _Grid(*[int(v) for v in grid[:3]], *[float(v) for v in tuple(grid)[3:9]],
+                      pts.ctypes.data_as(ctypes.c_void_p))
+            _check(lib().das_plan_create(ctypes.byref(h), ctypes.byref(g),
+                                         rx.ctypes.data_as(ctypes.c_void_p), c, fs, t0, fnum, dt,
+                                         self.B, self.Q, self.M, self.K))
+        elif points is not None:
             pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 3)
             self.grid = None
             self.N = pts.shape[0]
