@@ -157,9 +157,11 @@ das_status das_plan_create(das_plan *plan, const das_grid *grid, const float *rx
  * tau_tx / w_tx arrays are indexed by list position n.
  *   voxel_xyz  host, N x 3 float32 positions (metres), copied.
  *   other arguments as das_plan_create.
- * The brick and window kernels take bricks of consecutive list entries (the
- * window kernel quads of four), so ordering the list so that neighbours in it
- * are neighbours in space keeps their caches warm and the windows short.
+ * The plan keeps the list in its own spatially compact order (depth bands,
+ * deepest first, then a Morton curve in x-y on cells of the list's mean
+ * spacing), so the bricks of the brick and window kernels are neighbours in
+ * space whatever order the caller lists the voxels in; y, tau_tx and w_tx
+ * stay in the caller's order.
  * Errors: as das_plan_create.
  */
 das_status das_plan_create_points(das_plan *plan, const float *voxel_xyz, int N,

@@ -56,6 +56,48 @@ def test_sampled_grid_voxels_as_a_list(oracle, base, kernel):
     assert np.abs(y - y_grid[:, idx]).max() <= TOL * np.abs(y_grid).max()
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_list_order_does_not_change_the_result(kernel):
+    """The plan keeps a list in its own compact order; permuting the caller's
+    list permutes y and nothing else: bit for bit where each voxel's sum runs
+    in the same order wherever it lands (BL, BI, brick), to float32 rounding
+    for the window kernel (its passes run over the receivers active for the
+    warp's voxels, so the order of the terms depends on the neighbours)."""
+    prob = synth.make_problem("full", n_el=8, nx=19, ny=13, nz=5)
+    rng = np.random.default_rng(24)
+    idx = rng.choice(prob.N, 400, replace=False)
+    perm = rng.permutation(len(idx))
+    runs = []
+    for sel in (idx, idx[perm]):
+        pts = synth.grid_points(prob.grid, sel).astype(np.float32)
+        runs.append(run_points(prob, pts, prob.tau_tx[:, sel], prob.w_tx[:, sel], kernel))
+    if kernel == "window":
+        assert np.abs(runs[0][:, perm] - runs[1]).max() <= 1e-5 * np.abs(runs[1]).max()
+    else:
+        assert np.array_equal(runs[0][:, perm], runs[1])
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_degenerate_lists(oracle, kernel):
+    """Lists the ordering cannot spread out: one point, repeated points, a
+    flat sheet (one depth), a line."""
+    prob = synth.make_problem("mid", n_el=8, nx=4, ny=4, nz=4, B=16)
+    wl = prob.wl
+    rng = np.random.default_rng(25)
+    sheet = np.column_stack([rng.uniform(-2e-3, 2e-3, 70), rng.uniform(-2e-3, 2e-3, 70),
+                             np.full(70, 12e-3)])
+    line = np.column_stack([np.zeros(37), np.zeros(37), np.linspace(5e-3, 25e-3, 37)])
+    cases = {"one": np.array([[0.0, 0.0, 10e-3]]), "repeated": np.tile([[1e-3, -1e-3, 15e-3]], (33, 1)),
+             "sheet": sheet, "line": line}
+    for name, pts in cases.items():
+        pts = pts.astype(np.float32)
+        tau = synth.transmit_delays(wl, pts.astype(np.float64)).astype(np.float32)
+        w = rng.uniform(0.5, 1.0, (wl.Q, len(pts))).astype(np.float32)
+        y = run_points(prob, pts, tau, w, kernel)
+        ref, slack = oracle_points(oracle, prob, pts, tau, w)
+        assert error_ratio(y, ref, slack) <= TOL, (name, kernel)
+
+
 def test_list_through_the_grid_struct_matches_points_plan():
     """das_plan_create with grid.xyz set builds the same plan as
     das_plan_create_points: identical output, bit for bit."""

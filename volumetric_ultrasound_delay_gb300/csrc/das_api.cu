@@ -1,8 +1,10 @@
 // C ABI of libdas: plan management, argument checks and kernel dispatch.
 // Every entry point validates on the host, launches nothing when it rejects a
 // call, and maps CUDA failures to DAS_ERR_CUDA with a readable message.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
+#include <cstdint>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -52,7 +54,8 @@ struct das_plan_s {
     bool last_had_permute = false;
     cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
     RxPos *d_rx = nullptr;
-    float4 *d_vox = nullptr;                  // voxel list (sample units), list plans only
+    float4 *d_vox = nullptr;                  // voxel list (sample units, slot order), list plans only
+    int *d_order = nullptr;                   // list plans: caller's index of each slot
     Pos64 *d_rx64 = nullptr, *d_vox64 = nullptr;   // double copies, float64 / complex128 plans
     void *d_perm = nullptr;
     size_t perm_bytes = 0;
@@ -87,6 +90,55 @@ int resolve_kernel(const das_plan_s *p)
     if (das::brick_supported(p->B, cplx, p->K)) return DAS_KERNEL_BRICK;
     if (p->K >= 2 && das::bi_supported(p->B, cplx, p->bi_group)) return DAS_KERNEL_BI;
     return DAS_KERNEL_BL;
+}
+
+// Order in which a voxel list plan keeps its voxels: deepest first in depth
+// bands, then along a 2-D Morton curve in x-y, on cells of the list's mean
+// spacing.  Neighbouring slots are then neighbours in space, as the bricks of
+// a grid are (same rows of the record, warm caches), whatever order the
+// caller lists them in.  Returns an empty vector when the points span no
+// volume worth ordering (then slot = index).
+std::vector<int> compact_order(const float *xyz, int N)
+{
+    std::vector<int> order;
+    if (N < 2) return order;
+    double lo[3] = {xyz[0], xyz[1], xyz[2]}, hi[3] = {xyz[0], xyz[1], xyz[2]};
+    for (int n = 1; n < N; ++n)
+        for (int d = 0; d < 3; ++d) {
+            lo[d] = std::min(lo[d], (double)xyz[3 * n + d]);
+            hi[d] = std::max(hi[d], (double)xyz[3 * n + d]);
+        }
+    // mean spacing: the cube root of the volume per point, over the extents
+    // that are not flat
+    double vol = 1.0;
+    int dims = 0;
+    for (int d = 0; d < 3; ++d)
+        if (hi[d] > lo[d]) { vol *= hi[d] - lo[d]; ++dims; }
+    if (dims == 0) return order;
+    const double h = std::pow(vol / N, 1.0 / dims);
+    if (!(h > 0.0) || !std::isfinite(h)) return order;
+    auto cell = [&](double v, double origin) -> uint32_t {
+        const double c = std::floor((v - origin) / h);
+        return c <= 0.0 ? 0u : (c >= 65535.0 ? 65535u : (uint32_t)c);
+    };
+    auto spread = [](uint32_t v) -> uint64_t {   // bit i of v to bit 2i
+        uint64_t x = v & 0xffffu;
+        x = (x | (x << 8)) & 0x00ff00ffull;
+        x = (x | (x << 4)) & 0x0f0f0f0full;
+        x = (x | (x << 2)) & 0x33333333ull;
+        x = (x | (x << 1)) & 0x55555555ull;
+        return x;
+    };
+    std::vector<uint64_t> key(N);
+    for (int n = 0; n < N; ++n) {
+        const uint64_t band = cell(hi[2] - (double)xyz[3 * n + 2], 0.0);   // 0 = deepest
+        key[n] = (band << 32) | (spread(cell(xyz[3 * n], lo[0])) |
+                                 (spread(cell(xyz[3 * n + 1], lo[1])) << 1));
+    }
+    order.resize(N);
+    for (int n = 0; n < N; ++n) order[n] = n;
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return key[a] < key[b]; });
+    return order;
 }
 
 das_status check_supported(const das_plan_s *p, int kernel)
@@ -125,6 +177,7 @@ void release(das_plan_s *p)
 {
     cudaFree(p->d_rx);
     cudaFree(p->d_vox);
+    cudaFree(p->d_order);
     cudaFree(p->d_rx64);
     cudaFree(p->d_vox64);
     cudaFree(p->d_perm);
@@ -300,13 +353,22 @@ das_status das_plan_create_points(das_plan *plan, const float *voxel_xyz, int N,
     if (st != DAS_OK) return st;
     das_plan_s *p = *plan;
     const double s = (double)fs / (double)c;
+    // slot k holds voxel order[k]; positions are uploaded in slot order
+    const std::vector<int> order = compact_order(voxel_xyz, N);
+    auto index = [&](int k) { return order.empty() ? k : order[k]; };
     std::vector<float4> hv(N);
-    for (int n = 0; n < N; ++n)
-        hv[n] = make_float4((float)(voxel_xyz[3 * n] * s), (float)(voxel_xyz[3 * n + 1] * s),
-                            (float)(voxel_xyz[3 * n + 2] * s), 0.f);
+    for (int k = 0; k < N; ++k) {
+        const float *v = voxel_xyz + 3 * (size_t)index(k);
+        hv[k] = make_float4((float)(v[0] * s), (float)(v[1] * s), (float)(v[2] * s), 0.f);
+    }
     cudaError_t e = cudaMalloc(&p->d_vox, sizeof(float4) * (size_t)N);
     if (e == cudaSuccess)
         e = cudaMemcpy(p->d_vox, hv.data(), sizeof(float4) * (size_t)N, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && !order.empty()) {
+        e = cudaMalloc(&p->d_order, sizeof(int) * (size_t)N);
+        if (e == cudaSuccess)
+            e = cudaMemcpy(p->d_order, order.data(), sizeof(int) * (size_t)N, cudaMemcpyHostToDevice);
+    }
     if (e != cudaSuccess) {
         das_plan_destroy(p);
         *plan = nullptr;
@@ -314,10 +376,14 @@ das_status das_plan_create_points(das_plan *plan, const float *voxel_xyz, int N,
         return cuda_fail(e, "voxel list upload");
     }
     p->geom.vox = p->d_vox;
+    p->geom.order = p->d_order;
+    p->geom64.order = p->d_order;
     if (p->is_double()) {
         std::vector<Pos64> h64(N);
-        for (int n = 0; n < N; ++n)
-            h64[n] = Pos64{voxel_xyz[3 * n] * s, voxel_xyz[3 * n + 1] * s, voxel_xyz[3 * n + 2] * s, 0.0};
+        for (int k = 0; k < N; ++k) {
+            const float *v = voxel_xyz + 3 * (size_t)index(k);
+            h64[k] = Pos64{v[0] * s, v[1] * s, v[2] * s, 0.0};
+        }
         e = cudaMalloc(&p->d_vox64, sizeof(Pos64) * (size_t)N);
         if (e == cudaSuccess)
             e = cudaMemcpy(p->d_vox64, h64.data(), sizeof(Pos64) * (size_t)N, cudaMemcpyHostToDevice);
@@ -571,6 +637,7 @@ das_status das_plan_device_bytes(das_plan p, size_t *bytes)
 {
     if (!p || !bytes) return fail(DAS_ERR_INVALID_ARG, "NULL argument");
     size_t b = sizeof(RxPos) * p->M + p->perm_bytes + (p->d_vox ? sizeof(float4) * (size_t)p->N : 0);
+    if (p->d_order) b += sizeof(int) * (size_t)p->N;
     if (p->d_rx64) b += sizeof(Pos64) * p->M;
     if (p->d_vox64) b += sizeof(Pos64) * (size_t)p->N;
     if (p->d_rf) b += p->rf_bytes();

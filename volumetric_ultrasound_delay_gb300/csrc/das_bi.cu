@@ -29,9 +29,10 @@ das_bi_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__
     const int warp = threadIdx.x >> 5;
     const int grp = lane / G;
     const int t = lane % G;
-    const int n = (blockIdx.x * (THREADS / 32) + warp) * NW + grp;
-    const bool nvalid = n < g.N;
-    const float3 p = nvalid ? voxel_position(g, n) : make_float3(0.f, 0.f, 0.f);
+    const int s = (blockIdx.x * (THREADS / 32) + warp) * NW + grp;   // voxel slot
+    const bool nvalid = s < g.N;
+    const float3 p = nvalid ? voxel_position(g, s) : make_float3(0.f, 0.f, 0.f);
+    const int n = nvalid ? voxel_index(g, s) : 0;
     const long long qmb = (long long)g.Q * g.M * g.B;        // row stride of k
     const T *permT = reinterpret_cast<const T *>(perm);
 

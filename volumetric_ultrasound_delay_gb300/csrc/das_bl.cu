@@ -24,11 +24,12 @@ das_bl_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__
     using T = typename std::conditional<CPLX, float2, float>::type;
     const T *rfT = reinterpret_cast<const T *>(rf);
     T *outT = reinterpret_cast<T *>(out);
-    const int n = blockIdx.x * THREADS + threadIdx.x;
+    const int s = blockIdx.x * THREADS + threadIdx.x;   // voxel slot
     const int b0 = blockIdx.y * B_TILE;
-    if (n >= g.N) return;
+    if (s >= g.N) return;
     const int nb = min(B_TILE, g.B - b0);
-    const float3 p = voxel_position(g, n);
+    const float3 p = voxel_position(g, s);
+    const int n = voxel_index(g, s);
     const long long b_stride = (long long)g.Q * g.M * g.K;
 
     T acc[B_TILE];
@@ -92,13 +93,14 @@ das_bl64_kernel(DasGeom64 g, const Pos64 *__restrict__ rx, const void *__restric
     using T = typename std::conditional<CPLX, double2, double>::type;
     const T *rfT = static_cast<const T *>(rf);
     T *outT = static_cast<T *>(out);
-    const int n = blockIdx.x * THREADS + threadIdx.x;
+    const int s = blockIdx.x * THREADS + threadIdx.x;   // voxel slot
     const int b0 = blockIdx.y * B_TILE;
-    if (n >= g.N) return;
+    if (s >= g.N) return;
     const int nb = min(B_TILE, g.B - b0);
+    const int n = g.order ? __ldg(g.order + s) : s;
     double px, py, pz;
     if (g.vox) {
-        px = g.vox[n].x; py = g.vox[n].y; pz = g.vox[n].z;
+        px = g.vox[s].x; py = g.vox[s].y; pz = g.vox[s].z;
     } else {
         const int ix = n % g.nx, iy = (n / g.nx) % g.ny, iz = n / (g.nx * g.ny);
         px = g.x0 + ix * g.dx; py = g.y0 + iy * g.dy; pz = g.z0 + iz * g.dz;

@@ -255,6 +255,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                 const float4 p = __ldg(g.vox + n);
                 *pos = make_float3(p.x, p.y, p.z);
             }
+            n = voxel_index(g, n);     // slot -> the caller's index
             return true;
         }
         const int ix = bx * BX + v % BX, iy = by * (V / BX) + v / BX;

@@ -11,6 +11,15 @@
 
 namespace das {
 
+// Voxel list plans keep the list in a spatially compact order: slot s holds
+// the voxel the caller lists at index order[s] (tau_tx, w_tx and y use that
+// index).  Grid plans: slot = index.
+__device__ __forceinline__ int voxel_index(const DasGeom &g, int s)
+{
+    return g.order ? __ldg(g.order + s) : s;
+}
+
+// position of the voxel in slot n (grid plans: voxel n), sample units
 __device__ __forceinline__ float3 voxel_position(const DasGeom &g, int n)
 {
     if (g.vox) {

@@ -21,7 +21,8 @@ struct DasGeom {
     float fd_over_fs;     // demodulation cycles per sample (IQ)
     int rotate;           // 1: apply the IQ phase
     int B, Q, M, K;
-    const float4 *vox;    // voxel list (sample units), or nullptr for the regular grid
+    const float4 *vox;    // voxel list (sample units) in slot order, or nullptr for the grid
+    const int *order;     // list plans: caller's index of the voxel in each slot
 };
 
 // Receiver record of the plan: position in sample units.
@@ -39,7 +40,8 @@ struct DasGeom64 {
     double fs, t0fs, ap2, fd_over_fs;
     int aperture;
     int B, Q, M, K;
-    const Pos64 *vox;     // voxel list (sample units), or nullptr for the grid
+    const Pos64 *vox;     // voxel list (sample units) in slot order, or nullptr for the grid
+    const int *order;     // list plans: caller's index of the voxel in each slot
 };
 
 namespace das {

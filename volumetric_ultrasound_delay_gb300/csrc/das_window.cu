@@ -140,6 +140,7 @@ das_window_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restri
                 const float4 p = __ldg(g.vox + n);
                 *pos = make_float3(p.x, p.y, p.z);
             }
+            n = voxel_index(g, n);     // slot -> the caller's index
             return true;
         }
         const int j = v & 3, qd = (v >> 2) % NQ, w = (v >> 2) / NQ;
