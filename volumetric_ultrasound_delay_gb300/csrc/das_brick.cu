@@ -1,10 +1,14 @@
 // BRICK: this library's DAS kernel for sm_103a (not a design from the pages).
 //
-// Each CTA (8 warps) owns a brick of V voxels in one x-y slice (8 x 4 for 32
-// frames of float32) and all B frames of them.  Neighbouring voxels of a slice
-// need nearly the same sample rows of every receiver, so the warps of a CTA
-// walking the same receivers at the same time hit the same L1 lines; bricks are
-// flat in z because one voxel step in depth moves the delay by many samples.
+// Each CTA (WARPS warps, one by default) owns a brick of V voxels in one x-y
+// slice (4 x 1 for 32 frames of float32 with one warp) and all B frames of
+// them.  Neighbouring voxels of a slice need nearly the same sample rows of
+// every receiver, so the groups of a warp walking the same receivers at the
+// same time hit the same L1 lines; bricks are flat in z because one voxel step
+// in depth moves the delay by many samples.  One-warp CTAs measured fastest
+// (32-frame float32 volume: 8 warps 13.8 ms, 4 13.2, 2 13.0, 1 12.5): the
+// transmit-delay preload needs no CTA-wide barrier wait, and the scheduler
+// balances finer pieces of work.
 //
 // The record is permuted to the zero-padded layout Q x M x (K+3) x B (sample k
 // of slab (q, m) at row k + 1, rows 0, K+1, K+2 zero), so the two rows a voxel
@@ -44,16 +48,16 @@
 #include "das_device.cuh"
 
 // tuning (float32 storage, one chunk per lane): receivers per phase-C trip
-// and the CTAs per SM the register allocation must allow; half storage keeps
-// 2 receivers per trip and 5 CTAs per SM; and the warps per CTA
+// and the warps per SM the register allocation must allow; half storage keeps
+// 2 receivers per trip and 40 warps per SM; and the warps per CTA
 #ifndef DAS_BRICK_U1
 #define DAS_BRICK_U1 4
 #endif
-#ifndef DAS_BRICK_MIN_BLOCKS
-#define DAS_BRICK_MIN_BLOCKS 4
+#ifndef DAS_BRICK_MIN_WARPS
+#define DAS_BRICK_MIN_WARPS 32
 #endif
 #ifndef DAS_BRICK_WARPS
-#define DAS_BRICK_WARPS 8
+#define DAS_BRICK_WARPS 1
 #endif
 #ifndef DAS_BRICK_PACKED
 #define DAS_BRICK_PACKED 1     // real entries packed into 32 bits (else {row, fraction} floats)
@@ -71,7 +75,8 @@ constexpr float FAR = 1.0e30f;         // distance marking "outside the aperture
 // footprint in y is V / BX
 template <int V>
 struct BrickShape {
-    static constexpr int BX = V >= 512 ? 32 : (V >= 128 ? 16 : (V >= 32 ? 8 : 4));
+    static constexpr int BX = V >= 512 ? 32 : (V >= 128 ? 16 : (V >= 32 ? 8 : (V >= 4 ? 4 : V)));
+    static_assert(V >= 1 && (V & (V - 1)) == 0 && V % BX == 0, "bricks tile V voxels");
 };
 
 // Real entry: one 32-bit word, the row relative to the first row of the block
@@ -193,15 +198,24 @@ __device__ __forceinline__ void accumulate(float2 (&acc)[NA][NP], float wq, floa
     }
 }
 
-// CTAs per SM the register allocation must allow: lanes that hold more chunks
-// (J) or complex samples keep more row data in flight per trip; 16-lane groups
-// (at most two chunks a lane) fit 4 CTAs per SM, 3 for complex with 4 entries
-// per trip
+// Warps per SM the register allocation must allow: lanes that hold more
+// chunks (J) or complex samples keep more row data in flight per trip, so
+// they get fewer warps (more registers each); 16-lane groups (at most two
+// chunks a lane) fit 32 warps, 24 for complex with 4 entries per trip.  The
+// CTA count per SM is that over the warps per CTA.
+template <int G, int J, bool CPLX, bool HALF>
+constexpr int min_warps()
+{
+    return G == 16 ? (CPLX && J == 1 ? 24 : 32)
+                   : (J >= 4 ? 16 : (J == 2 || CPLX ? 24 : (HALF ? 40 : DAS_BRICK_MIN_WARPS)));
+}
 template <int G, int J, bool CPLX, bool HALF>
 constexpr int min_blocks()
 {
-    return G == 16 ? (CPLX && J == 1 ? 3 : 4)
-                   : (J >= 4 ? 2 : (J == 2 || CPLX ? 3 : (HALF ? 5 : DAS_BRICK_MIN_BLOCKS)));
+    // at least 1, at most the 32 resident CTAs an SM holds
+    return min_warps<G, J, CPLX, HALF>() / WARPS < 1
+               ? 1
+               : (min_warps<G, J, CPLX, HALF>() / WARPS > 32 ? 32 : min_warps<G, J, CPLX, HALF>() / WARPS);
 }
 
 // receivers per phase-C trip
