@@ -509,8 +509,9 @@ cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, cons
 // Lanes per voxel G, chunks J, and split mode for B frames.
 //   float32 / complex64 storage: pair mode, CPR = B * size / 16 chunks per row,
 //     G = CPR if <= 8 (J = 1); rows of 16 or 32 chunks G = 16, J = CPR / 16
-//     (16 lanes at one or two chunks each leave room for 4 CTAs per SM, where
-//     8 lanes at four chunks fit only 2); else G = 8, J = CPR / 8 in {2, 4};
+//     (16 lanes at one or two chunks each leave room for 32 warps per SM,
+//     where 8 lanes at four chunks fit only 16); else G = 8, J = CPR / 8 in
+//     {2, 4};
 //   half / half2 storage: rows of <= 64 bytes (CPR <= 4) use split mode with
 //     G = 2 CPR; wider rows pair mode with G = 8, J = CPR / 8 in {1, 2}.
 bool choose(int B, bool cplx, bool half, int &G, int &J, bool &split)
