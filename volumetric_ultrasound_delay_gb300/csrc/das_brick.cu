@@ -47,9 +47,9 @@
 
 #include "das_device.cuh"
 
-// tuning (float32 storage, one chunk per lane): receivers per phase-C trip
-// and the warps per SM the register allocation must allow; half storage keeps
-// 2 receivers per trip and 40 warps per SM; and the warps per CTA
+// tuning (one chunk per lane, float32 or half storage): receivers per
+// phase-C trip and the warps per SM the register allocation must allow; and
+// the warps per CTA
 #ifndef DAS_BRICK_U1
 #define DAS_BRICK_U1 4
 #endif
@@ -207,7 +207,7 @@ template <int G, int J, bool CPLX, bool HALF>
 constexpr int min_warps()
 {
     return G == 16 ? (CPLX && J == 1 ? 24 : 32)
-                   : (J >= 4 ? 16 : (J == 2 || CPLX ? 24 : (HALF ? 40 : DAS_BRICK_MIN_WARPS)));
+                   : (J >= 4 ? 16 : (J == 2 || CPLX ? 24 : DAS_BRICK_MIN_WARPS));
 }
 template <int G, int J, bool CPLX, bool HALF>
 constexpr int min_blocks()
@@ -220,7 +220,7 @@ constexpr int min_blocks()
 
 // receivers per phase-C trip
 template <int J, bool HALF>
-constexpr int trip_size() { return J >= 4 ? 1 : (J == 2 ? 2 : (HALF ? 2 : DAS_BRICK_U1)); }
+constexpr int trip_size() { return J >= 4 ? 1 : (J == 2 ? 2 : DAS_BRICK_U1); }
 
 template <int G, int J, bool CPLX, bool HALF, bool SPLIT>
 __global__ void __launch_bounds__(THREADS, min_blocks<G, J, CPLX, HALF>())
