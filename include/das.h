@@ -80,7 +80,9 @@ typedef enum {
                               a group of lanes owns a 2 x 2 quad of voxels and loads
                               the window of rows the quad needs for a (transmit,
                               receiver) once, with one coefficient per voxel and row.
-                              float32 records with B in {8, 16, 32} only; on request
+                              float32 records with B in {8, 16, 32} only; a non-finite
+                              sample reaches every voxel of a quad whose window holds its
+                              row (zero weight times inf/NaN); on request
                               (AUTO keeps the brick kernel, faster on the workloads
                               measured so far) */
 } das_kernel;
