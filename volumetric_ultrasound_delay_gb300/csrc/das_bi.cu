@@ -15,7 +15,7 @@
 namespace das {
 namespace {
 
-constexpr int THREADS = 256;
+constexpr int THREADS = 64;     // 2 warps: 5 % faster than 256 on the 32 x 32-array volume
 
 template <int G, int J, bool CPLX>
 __global__ void __launch_bounds__(THREADS)
