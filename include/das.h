@@ -237,7 +237,9 @@ das_status das_plan_destroy(das_plan plan);
  *   in       device buffer of B*Q*M*K elements of dtype;
  *   out      device buffer of B*Q*M*K (layouts 0, 1) or B*Q*M*(K+3) (layout 2)
  *            elements of dtype, or of half / half2 with DAS_STORAGE_F16; in and
- *            out must not overlap.
+ *            out must not overlap, and each must be aligned to its element
+ *            size (16-byte alignment, with K and B multiples of a 16-byte
+ *            vector, selects the vectorised loads and stores).
  * Errors: DAS_ERR_INVALID_ARG, DAS_ERR_CUDA.  Asynchronous.
  */
 das_status das_permute(const void *in, void *out, das_dtype dtype, int B, int Q, int M,
@@ -248,7 +250,7 @@ das_status das_permute(const void *in, void *out, das_dtype dtype, int B, int Q,
  * bit (ffdas paper, Methods, batch-inner paragraph; ffdas docs, ALG2, the
  * permute done as part of the launch).  Same as das_permute with layout 0 and
  * DAS_STORAGE_NATIVE: dtype DAS_F32 or DAS_C64, in and out device buffers of
- * B*Q*M*K elements that must not overlap.
+ * B*Q*M*K elements, aligned to the element size, that must not overlap.
  * Errors: DAS_ERR_INVALID_ARG, DAS_ERR_CUDA.  Asynchronous.
  */
 das_status das_permute_bqmk_to_kqmb(const void *in, void *out, das_dtype dtype, int B, int Q,

@@ -70,6 +70,16 @@ def test_host_side_rejections(libdas):
     assert libdas.das_permute(buf, buf, 0, 1, 1, 1, 4, 0, 0, None) == das.DAS_ERR_INVALID_ARG  # overlap
     assert libdas.das_permute(buf, ctypes.byref(buf, 32), 0, 1, 1, 1, 4, 3, 0, None) == das.DAS_ERR_INVALID_ARG  # bad layout
     assert libdas.das_permute(buf, ctypes.byref(buf, 32), 0, 1, 1, 1, 4, 0, 7, None) == das.DAS_ERR_INVALID_ARG  # bad storage
+    # element alignment: float32 needs 4 bytes, complex64 8, a half copy 2
+    base = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 16
+    big = ctypes.create_string_buffer(256)
+    bbase = ctypes.addressof(big) + (-ctypes.addressof(big)) % 16
+    assert libdas.das_permute(base + 2, bbase, 0, 1, 1, 1, 4, 0, 0, None) == das.DAS_ERR_INVALID_ARG
+    assert b"aligned" in libdas.das_last_error_string()
+    assert libdas.das_permute(base, bbase + 1, 0, 1, 1, 1, 4, 0, 0, None) == das.DAS_ERR_INVALID_ARG
+    assert libdas.das_permute(base + 4, bbase, 1, 1, 1, 1, 2, 0, 0, None) == das.DAS_ERR_INVALID_ARG
+    assert libdas.das_permute(base, bbase + 1, 0, 1, 1, 1, 4, 0, 1, None) == das.DAS_ERR_INVALID_ARG
+    assert libdas.das_permute_bqmk_to_kqmb(base + 2, bbase, 0, 1, 1, 1, 4, None) == das.DAS_ERR_INVALID_ARG
     assert libdas.das_permute_bqmk_to_kqmb(None, None, 0, 1, 1, 1, 1, None) == das.DAS_ERR_INVALID_ARG
     assert libdas.das_permute_bqmk_to_kqmb(buf, buf, 0, 1, 1, 1, 4, None) == das.DAS_ERR_INVALID_ARG  # overlap
     assert libdas.das_permute_bqmk_to_kqmb(buf, ctypes.byref(buf, 32), 5, 1, 1, 1, 4, None) == das.DAS_ERR_INVALID_ARG

@@ -673,7 +673,11 @@ das_status das_permute(const void *in, void *out, das_dtype dtype, int B, int Q,
     const bool half = storage == DAS_STORAGE_F16;
     const size_t eb = dtype == DAS_C64 ? 8 : 4;
     const size_t bytes = (size_t)B * Q * M * K * eb;
-    const size_t obytes = (size_t)B * Q * M * (K + (layout == 2 ? 3 : 0)) * (half ? eb / 2 : eb);
+    const size_t oeb = half ? eb / 2 : eb;
+    if ((reinterpret_cast<uintptr_t>(in) % eb) != 0 || (reinterpret_cast<uintptr_t>(out) % oeb) != 0)
+        return fail(DAS_ERR_INVALID_ARG, "in and out must be aligned to their element sizes (%zu, %zu bytes)",
+                    eb, oeb);
+    const size_t obytes = (size_t)B * Q * M * (K + (layout == 2 ? 3 : 0)) * oeb;
     const char *a = static_cast<const char *>(in);
     const char *b = static_cast<const char *>(out);
     if (a < b + obytes && b < a + bytes) return fail(DAS_ERR_INVALID_ARG, "in and out overlap");
