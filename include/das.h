@@ -71,7 +71,10 @@ typedef enum {
                               ffdas docs, ALG1) */
     DAS_KERNEL_BI = 2,     /* batch-inner warp tiling on a K x Q x M x B copy
                               (ffdas paper, Methods, batch-inner paragraphs /
-                              Algorithm 2; ffdas docs, ALG2) */
+                              Algorithm 2; ffdas docs, ALG2); the transmit delays
+                              and weights of a CTA's voxels sit in shared memory,
+                              so Q is limited to 227 KB / (8 B x voxels per CTA),
+                              at least 908 */
     DAS_KERNEL_BRICK = 3,  /* this library's sm_103a design: voxel bricks per CTA,
                               per-(voxel, transmit, receiver) geometry staged in
                               shared memory, receivers outside every aperture of

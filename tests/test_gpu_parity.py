@@ -211,6 +211,43 @@ def test_unsupported_requests_are_rejected():
     plan.close()
 
 
+def test_bi_transmit_table_limit(oracle):
+    """BI keeps its CTA's transmit table in shared memory: with more transmits
+    than fit it rejects the plan, and AUTO serves it with the brick kernel;
+    AUTO and the per-voxel baseline match the oracle."""
+    import oracle as oracle_mod
+    from volumetric_ultrasound_delay_gb300 import das
+    B, Q, M, K = 8, 1000, 1, 8
+    rng = np.random.default_rng(11)
+    grid = (2, 2, 1, -1e-3, -1e-3, 10e-3, 2e-3, 2e-3, 1e-3)
+    rx = np.zeros((M, 3), np.float32)
+    rf = torch.from_numpy(rng.standard_normal((B, Q, M, K)).astype(np.float32)).cuda()
+    # every voxel is 10.0995 mm from the receiver: delays that land inside the
+    # 8-sample record, f = (tau + d / c) * fs in [1, 6]
+    d = np.sqrt(1e-6 + 1e-6 + 100e-6)
+    tau_np = (-d / 1540.0 + rng.uniform(1.0, 6.0, (Q, 4)) / 20e6).astype(np.float32)
+    tau = torch.from_numpy(tau_np).cuda()
+    w = torch.from_numpy(rng.uniform(0.5, 1.0, (Q, 4)).astype(np.float32)).cuda()
+    ys = {}
+    for kernel in ("bi", "auto", "bl"):
+        plan = das.Plan(grid, rx, 1540.0, 20e6, 0.0, 0.0, "f32", B, Q, M, K, kernel=kernel)
+        if kernel == "bi":
+            with pytest.raises(das.DasError) as exc:
+                plan.beamform(rf, tau, w)
+            assert exc.value.status == das.DAS_ERR_UNSUPPORTED
+        else:
+            if kernel == "auto":
+                assert plan.kernel == "brick"
+            ys[kernel] = plan.beamform(rf, tau, w).cpu().numpy()
+        plan.close()
+    ref, slack = oracle.beamform(rf.cpu().numpy(), tau.cpu().numpy(), w.cpu().numpy(),
+                                 rx.astype(np.float64), oracle_mod.Grid(*grid), c=1540.0, fs=20e6,
+                                 t0=0.0, fnum=0.0, want_slack=True)
+    assert np.abs(ref).max() > 0
+    for kernel, y in ys.items():
+        assert error_ratio(y, ref, slack) <= TOL, (kernel, error_ratio(y, ref, slack))
+
+
 def test_misaligned_and_wrong_sizes_rejected():
     from volumetric_ultrasound_delay_gb300 import das
     prob = _custom(B=8)

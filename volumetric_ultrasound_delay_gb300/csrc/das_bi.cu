@@ -5,17 +5,32 @@
 // holds the 16-byte chunks t, t + G, t + 2G, ... of b, so at every (k, q, m)
 // the group reads G consecutive 16-byte vectors (full 32-byte sectors).
 //
-// Geometry is spread over the group and shared by warp shuffles: for each
-// transmit q and each block of G receivers, lane t works out the row, the two
-// interpolation weights (and, for IQ, the phase-rotated complex weights) of
-// receiver m0 + t, then the group walks the G receivers, broadcasting each
-// receiver's values from its lane.
+// Geometry is spread over the group and shared by warp shuffles.  The CTA
+// first stages its voxels' transmit delays and weights in shared memory.  For
+// each block of G receivers, lane t works out the distance of receiver m0 + t
+// to the group's voxel and the F-number test once; then, per transmit q, the
+// lane turns them into a row and two interpolation weights (IQ: and the
+// demodulation phase).  A ballot gives each group the receivers of the block
+// that contribute, and the group walks only those, U at a time, broadcasting
+// each receiver's row and weights from its lane and issuing the row loads of
+// the U receivers before their FMAs.  Real frames are accumulated in pairs
+// with the packed FP32 FMA (__ffma2_rn).
 #include "das_device.cuh"
+
+#ifndef DAS_BI_U
+#define DAS_BI_U 2
+#endif
 
 namespace das {
 namespace {
 
-constexpr int THREADS = 64;     // 2 warps: 5 % faster than 256 on the 32 x 32-array volume
+constexpr int THREADS = 64;     // 2 warps per CTA
+
+// receivers per walk step: 2 for real data (32-frame float32 volume: 1 step
+// 30.0 ms, 2 21.7 ms, 4 28.9 ms); 1 for IQ, whose rows of 64 complex frames
+// leave no registers for a second receiver (65.7 ms against 75.9 ms)
+template <bool CPLX>
+constexpr int walk_step() { return CPLX ? 1 : DAS_BI_U; }
 
 template <int G, int J, bool CPLX>
 __global__ void __launch_bounds__(THREADS)
@@ -24,84 +39,144 @@ das_bi_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__
 {
     constexpr int NW = 32 / G;                    // voxels per warp
     constexpr int CH = CPLX ? 2 : 4;              // elements per 16-byte chunk
+    constexpr int U = walk_step<CPLX>();
     using T = typename std::conditional<CPLX, float2, float>::type;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int grp = lane / G;
     const int t = lane % G;
+    const unsigned gmask = G == 32 ? 0xffffffffu : ((1u << G) - 1u) << (grp * G);  // this group's lanes
     const int s = (blockIdx.x * (THREADS / 32) + warp) * NW + grp;   // voxel slot
     const bool nvalid = s < g.N;
     const float3 p = nvalid ? voxel_position(g, s) : make_float3(0.f, 0.f, 0.f);
     const int n = nvalid ? voxel_index(g, s) : 0;
     const long long qmb = (long long)g.Q * g.M * g.B;        // row stride of k
-    const T *permT = reinterpret_cast<const T *>(perm);
+    const T *permT = reinterpret_cast<const T *>(perm) + t * CH;
 
-    T acc[J][CH];
-#pragma unroll
-    for (int c = 0; c < J; ++c)
-#pragma unroll
-        for (int e = 0; e < CH; ++e) acc[c][e] = T{};
+    // per-voxel transmit delay (samples) and weight, once per CTA
+    extern __shared__ float2 txs[];     // [THREADS / 32 * NW][Q]
+    for (int e = threadIdx.x; e < (THREADS / 32) * NW * g.Q; e += THREADS) {
+        const int v = e / g.Q, q = e % g.Q;
+        const int sv = blockIdx.x * (THREADS / 32) * NW + v;
+        float2 val = make_float2(0.f, 0.f);
+        if (sv < g.N) {
+            const int nv = voxel_index(g, sv);
+            val = make_float2(fmaf(__ldg(tau + (long long)q * g.N + nv), g.fs, -g.t0fs),
+                              __ldg(wtx + (long long)q * g.N + nv));
+        }
+        txs[e] = val;
+    }
+    __syncthreads();
+    const float2 *txv = txs + (warp * NW + grp) * g.Q;
 
-    for (int q = 0; q < g.Q; ++q) {
-        const float wq = nvalid ? __ldg(wtx + (long long)q * g.N + n) : 0.f;
-        const float tq = nvalid ? fmaf(__ldg(tau + (long long)q * g.N + n), g.fs, -g.t0fs) : 0.f;
-        for (int m0 = 0; m0 < g.M; m0 += G) {
-            // ---- this lane's receiver m0 + t
-            const int m = m0 + t;
+    // real: frame pairs (2 per chunk); IQ: one complex frame each (2 per chunk)
+    float2 acc[J][2];
+#pragma unroll
+    for (int c = 0; c < J; ++c) acc[c][0] = acc[c][1] = make_float2(0.f, 0.f);
+
+    for (int m0 = 0; m0 < g.M; m0 += G) {
+        // ---- this lane's receiver m0 + t: distance and aperture, for every q
+        const int m = m0 + t;
+        float d = 0.f;
+        const bool ap = nvalid && m < g.M && receive_geometry(g, p, __ldg(rx + m), d);
+        if (__ballot_sync(0xffffffffu, ap) == 0u) continue;   // no voxel of the warp sees the block
+        for (int q = 0; q < g.Q; ++q) {
             int r0 = 0;
             float w0 = 0.f, w1 = 0.f;
             float2 ph = make_float2(1.f, 0.f);
-            if (nvalid && m < g.M) {
-                float d;
-                if (receive_geometry(g, p, __ldg(rx + m), d)) {
-                    const float f = tq + d;
-                    if (sample_pair(f, wq, g.K, r0, w0, w1) && CPLX) ph = demod_phase(g, f);
-                }
+            bool ok = false;
+            if (ap) {
+                const float2 tw = txv[q];
+                const float wq = tw.y;
+                const float f = tw.x + d;
+                ok = sample_pair(f, wq, g.K, r0, w0, w1);
+                if (CPLX && ok) ph = demod_phase(g, f);
             }
-            const int mcount = min(G, g.M - m0);     // warp-uniform
-            for (int j = 0; j < mcount; ++j) {
-                const int rj = __shfl_sync(0xffffffffu, r0, j, G);
-                const float a0 = __shfl_sync(0xffffffffu, w0, j, G);
-                const float a1 = __shfl_sync(0xffffffffu, w1, j, G);
-                float2 pj = make_float2(1.f, 0.f);
-                if constexpr (CPLX) {
-                    pj.x = __shfl_sync(0xffffffffu, ph.x, j, G);
-                    pj.y = __shfl_sync(0xffffffffu, ph.y, j, G);
-                }
-                if (a0 == 0.f && a1 == 0.f) continue;   // uniform within the group
-                const T *p0 = permT + (long long)rj * qmb + ((long long)q * g.M + m0 + j) * g.B;
-                const T *p1 = p0 + qmb;
+            // the group's contributing receivers of the block (same for all its lanes)
+            unsigned mine = __ballot_sync(0xffffffffu, ok) & gmask;
+            // element offset of row k = 0 of slab (q, m0 + j) is slab + (grp * G + j) * B
+            const long long slab = ((long long)q * g.M + m0 - grp * G) * g.B;
+            while (mine) {
+                // the next U receivers of the list (the lanes holding their values)
+                int src[U];
+                bool use[U];
+                src[0] = __ffs(mine) - 1;
+                use[0] = true;
+                mine &= mine - 1u;
 #pragma unroll
-                for (int c = 0; c < J; ++c) {
-                    const int b = (t + c * G) * CH;
+                for (int u = 1; u < U; ++u) {
+                    use[u] = mine != 0u;
+                    src[u] = use[u] ? __ffs(mine) - 1 : src[0];
+                    mine &= mine - 1u;
+                }
+                float4 v0[U][J], v1[U][J];
+                float2 W0[U], W1[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int rj = __shfl_sync(gmask, r0, src[u]);
+                    const float a0 = __shfl_sync(gmask, w0, src[u]);
+                    const float a1 = __shfl_sync(gmask, w1, src[u]);
+                    float2 pj = make_float2(1.f, 0.f);
                     if constexpr (CPLX) {
-                        const float4 u0 = __ldg(reinterpret_cast<const float4 *>(p0 + b));
-                        const float4 u1 = __ldg(reinterpret_cast<const float4 *>(p1 + b));
-                        const float2 W0 = make_float2(a0 * pj.x, a0 * pj.y);
-                        const float2 W1 = make_float2(a1 * pj.x, a1 * pj.y);
-                        cfma(acc[c][0], W0, make_float2(u0.x, u0.y));
-                        cfma(acc[c][1], W0, make_float2(u0.z, u0.w));
-                        cfma(acc[c][0], W1, make_float2(u1.x, u1.y));
-                        cfma(acc[c][1], W1, make_float2(u1.z, u1.w));
-                    } else {
-                        const float4 u0 = __ldg(reinterpret_cast<const float4 *>(p0 + b));
-                        const float4 u1 = __ldg(reinterpret_cast<const float4 *>(p1 + b));
-                        acc[c][0] = fmaf(a0, u0.x, fmaf(a1, u1.x, acc[c][0]));
-                        acc[c][1] = fmaf(a0, u0.y, fmaf(a1, u1.y, acc[c][1]));
-                        acc[c][2] = fmaf(a0, u0.z, fmaf(a1, u1.z, acc[c][2]));
-                        acc[c][3] = fmaf(a0, u0.w, fmaf(a1, u1.w, acc[c][3]));
+                        pj.x = __shfl_sync(gmask, ph.x, src[u]);
+                        pj.y = __shfl_sync(gmask, ph.y, src[u]);
+                    }
+                    W0[u] = CPLX ? make_float2(a0 * pj.x, a0 * pj.y) : make_float2(a0, a0);
+                    W1[u] = CPLX ? make_float2(a1 * pj.x, a1 * pj.y) : make_float2(a1, a1);
+                    const T *p0 = permT + (slab + (long long)rj * qmb + (long long)src[u] * g.B);
+#pragma unroll
+                    for (int c = 0; c < J; ++c) {
+                        v0[u][c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        v1[u][c] = v0[u][c];
+                        if (use[u]) {
+                            v0[u][c] = __ldg(reinterpret_cast<const float4 *>(p0 + c * G * CH));
+                            v1[u][c] = __ldg(reinterpret_cast<const float4 *>(p0 + qmb + c * G * CH));
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (!use[u]) break;
+#pragma unroll
+                    for (int c = 0; c < J; ++c) {
+                        const float2 x0 = make_float2(v0[u][c].x, v0[u][c].y), y0 = make_float2(v0[u][c].z, v0[u][c].w);
+                        const float2 x1 = make_float2(v1[u][c].x, v1[u][c].y), y1 = make_float2(v1[u][c].z, v1[u][c].w);
+                        if constexpr (CPLX) {
+                            cfma(acc[c][0], W1[u], x1);
+                            cfma(acc[c][1], W1[u], y1);
+                            cfma(acc[c][0], W0[u], x0);
+                            cfma(acc[c][1], W0[u], y0);
+                        } else {
+                            acc[c][0] = __ffma2_rn(W1[u], x1, acc[c][0]);
+                            acc[c][1] = __ffma2_rn(W1[u], y1, acc[c][1]);
+                            acc[c][0] = __ffma2_rn(W0[u], x0, acc[c][0]);
+                            acc[c][1] = __ffma2_rn(W0[u], y0, acc[c][1]);
+                        }
                     }
                 }
             }
         }
     }
     if (!nvalid) return;
-    T *outT = reinterpret_cast<T *>(out);
 #pragma unroll
-    for (int c = 0; c < J; ++c)
-#pragma unroll
-        for (int e = 0; e < CH; ++e) outT[(long long)((t + c * G) * CH + e) * g.N + n] = acc[c][e];
+    for (int c = 0; c < J; ++c) {
+        const long long e0 = (long long)(t + c * G) * CH;     // first element of the lane's chunk
+        if constexpr (CPLX) {
+            float2 *o = reinterpret_cast<float2 *>(out);
+            o[(e0 + 0) * g.N + n] = acc[c][0];
+            o[(e0 + 1) * g.N + n] = acc[c][1];
+        } else {
+            out[(e0 + 0) * g.N + n] = acc[c][0].x;
+            out[(e0 + 1) * g.N + n] = acc[c][0].y;
+            out[(e0 + 2) * g.N + n] = acc[c][1].x;
+            out[(e0 + 3) * g.N + n] = acc[c][1].y;
+        }
+    }
 }
+
+// shared memory of a CTA: the transmit table of its voxels
+size_t smem_bytes(int G, int Q) { return sizeof(float2) * (size_t)(THREADS / 32) * (32 / G) * Q; }
+constexpr size_t SMEM_MAX = 227 * 1024;
 
 template <int G, int J, bool CPLX>
 cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
@@ -110,7 +185,14 @@ cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, cons
     constexpr int NW = 32 / G;
     const int voxels_per_block = (THREADS / 32) * NW;
     const int grid = (g.N + voxels_per_block - 1) / voxels_per_block;
-    das_bi_kernel<G, J, CPLX><<<grid, THREADS, 0, stream>>>(
+    const size_t smem = smem_bytes(G, g.Q);
+    if (smem > SMEM_MAX) return cudaErrorInvalidValue;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(das_bi_kernel<G, J, CPLX>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    das_bi_kernel<G, J, CPLX><<<grid, THREADS, smem, stream>>>(
         g, rx, static_cast<const float *>(perm), tau, w, static_cast<float *>(out));
     return cudaGetLastError();
 }
@@ -131,10 +213,10 @@ bool choose(int B, bool cplx, int group, int &G, int &J)
 
 }  // namespace
 
-bool bi_supported(int B, bool cplx, int group)
+bool bi_supported(int B, bool cplx, int group, int Q)
 {
     int G, J;
-    return choose(B, cplx, group, G, J);
+    return choose(B, cplx, group, G, J) && smem_bytes(G, Q) <= SMEM_MAX;
 }
 
 cudaError_t launch_bi(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
