@@ -322,7 +322,20 @@ def pin_voxel_positions(orc):
     assert np.array_equal(xyz, expect), xyz
 
 
+def pin_hand_worked_examples(orc):
+    """The two delay-and-sum sums of tests/golden/ (record edges, the aperture,
+    the IQ phase and its sign), worked out by hand in the fixture."""
+    import golden_cases
+    for ex in golden_cases.examples():
+        rf, tau, w, rx = golden_cases.inputs(ex)
+        y = orc.beamform(rf, tau, w, rx.astype(np.float64), Grid(*ex["grid"]), c=ex["c"],
+                         fs=ex["fs"], t0=ex["t0"], fnum=ex["fnum"], f_demod=ex["f_demod"])
+        ref = golden_cases.expected(ex)
+        assert np.abs(y - ref).max() <= 1e-12 * np.abs(ref).max(), ex["name"]
+
+
 ALL_PINS = [
+    pin_hand_worked_examples,
     pin_impulse_interior, pin_impulse_upper_edge, pin_impulse_lower_edge,
     pin_iq_constant_record, pin_all_ones_aperture_count, pin_aperture_tie_slack,
     pin_bruteforce_real, pin_bruteforce_complex, pin_bruteforce_float64_records,
