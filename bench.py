@@ -15,6 +15,8 @@ Prints ONE JSON line (rank 0).  Besides the device-timed value it reports:
                 5 issue slots (2 loads + 3 FMA) per accumulation, B*N*Q*M
                 accumulations per launch; frac_in_aperture counts only the
                 accumulations inside the F-number aperture (the rest are zero);
+                diagnostics: the L1-return ceiling and the FMA floor over the
+                in-aperture accumulations;
   cpu_baseline  the float64 oracle on the host cores, on a bounded voxel sample;
   e2e           the same metric through das_beamform_host with pinned host
                 buffers (host->device and device->host copies inside the timing);
@@ -48,6 +50,7 @@ UNIT = "accumulations/s"
 ISSUE_SLOTS_PER_ACC = 5        # ~2 loads + 3 FMA per accumulation at FP32 issue peak
 FP32_LANES_PER_SM = 128
 L2_FALLBACK = 129 * 2**20       # GB300 L2 bytes, if the device properties do not say
+L1_BYTES_PER_CLK = 128          # L1 return to registers per SM and clock (one 128-byte wavefront)
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -397,6 +400,26 @@ def run_ours(args, world, rank, local):
                 "in_aperture_fraction": pairs / (prob.N * prob.M),
                 "peak_source": f"{props.multi_processor_count} SMs x {FP32_LANES_PER_SM} lanes x "
                                f"{sm_max:g} MHz ({peak_src})"}
+    # the two ceilings beside the issue roofline, over the in-aperture
+    # accumulations the kernels actually do: the L1 return of the samples
+    # (two rows of the frame's element per accumulation, at 128 B/clk/SM; the
+    # one that binds in practice) and the FMA floor (2 FMA per real
+    # accumulation with the weights folded, 8 per complex one, at 128/clk/SM)
+    sample_bytes = (2 if args.storage == "f16" else 4) * (2 if prob.wl.iq else 1)
+    sm_cycles = props.multi_processor_count * sm_max * 1e6            # SM clocks per second
+    l1_floor_ms = 1e3 * a_eff * 2 * sample_bytes / (sm_cycles * L1_BYTES_PER_CLK)
+    fma_per_acc = 8 if prob.wl.iq else 2
+    fma_floor_ms = 1e3 * a_eff * fma_per_acc / (sm_cycles * FP32_LANES_PER_SM)
+    roofline["diagnostics"] = {
+        "l1_return": {"bytes_per_accumulation": 2 * sample_bytes, "floor_ms": l1_floor_ms,
+                      "frac": l1_floor_ms / das_mean,
+                      "basis": f"{a_eff:.4g} in-aperture accumulations x {2 * sample_bytes} B at "
+                               f"{L1_BYTES_PER_CLK} B/clk/SM"},
+        "fma": {"fma_per_accumulation": fma_per_acc, "floor_ms": fma_floor_ms,
+                "frac": fma_floor_ms / das_mean,
+                "basis": f"{a_eff:.4g} in-aperture accumulations x {fma_per_acc} FMA at "
+                         f"{FP32_LANES_PER_SM}/clk/SM"},
+    }
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -38,6 +38,9 @@ def test_bench_line_carries_the_contract_keys():
         assert key in r, key
     assert r["bound"] == "alu" and r["achieved"] > 0 and r["peak"] > 0
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+    for ceiling in ("l1_return", "fma"):
+        c = r["diagnostics"][ceiling]
+        assert c["floor_ms"] > 0 and abs(c["frac"] - c["floor_ms"] / r["kernel_ms"]) < 1e-9
     e = d["e2e"]
     for key in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"):
         assert key in e, key
