@@ -74,7 +74,8 @@ typedef enum {
                               Algorithm 2; ffdas docs, ALG2); the transmit delays
                               and weights of a CTA's voxels sit in shared memory,
                               so Q is limited to 227 KB / (8 B x voxels per CTA),
-                              at least 908 */
+                              at least 908; rows are indexed in 32 bits of 16-byte
+                              chunks, so the record is below 64 GiB */
     DAS_KERNEL_BRICK = 3,  /* this library's sm_103a design: voxel bricks per CTA,
                               per-(voxel, transmit, receiver) geometry staged in
                               shared memory, receivers outside every aperture of

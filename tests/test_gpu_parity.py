@@ -248,6 +248,25 @@ def test_bi_transmit_table_limit(oracle):
         assert error_ratio(y, ref, slack) <= TOL, (kernel, error_ratio(y, ref, slack))
 
 
+def test_bi_chunk_index_limit():
+    """BI indexes rows in 32 bits of 16-byte chunks: a record of 2^34 chunks
+    (B = 64, M = 2^20, K = 1024) is rejected before anything is read, and AUTO
+    picks the brick kernel for it."""
+    from volumetric_ultrasound_delay_gb300 import das
+    B, Q, M, K = 64, 1, 1 << 20, 1024
+    rx = np.zeros((M, 3), np.float32)
+    plan = das.Plan((2, 2, 1, 0.0, 0.0, 0.01, 1e-3, 1e-3, 1e-3), rx, 1540.0, 20e6, 0.0, 1.5, "f32",
+                    B, Q, M, K)
+    assert plan.kernel == "brick"
+    plan.kernel = "bi"
+    dummy = torch.empty(1024, dtype=torch.float32, device="cuda")
+    st = das.lib().das_beamform(plan._h, dummy.data_ptr(), dummy.data_ptr(), dummy.data_ptr(),
+                                dummy.data_ptr() + 2048, None)
+    assert st == das.DAS_ERR_UNSUPPORTED
+    assert b"2^32" in das.lib().das_last_error_string()
+    plan.close()
+
+
 def test_misaligned_and_wrong_sizes_rejected():
     from volumetric_ultrasound_delay_gb300 import das
     prob = _custom(B=8)

@@ -88,7 +88,7 @@ int resolve_kernel(const das_plan_s *p)
     if (p->is_double()) return DAS_KERNEL_BL;                     // the only double-precision kernel
     if (p->storage == DAS_STORAGE_F16) return DAS_KERNEL_BRICK;   // the only half-storage kernel
     if (das::brick_supported(p->B, cplx, p->K)) return DAS_KERNEL_BRICK;
-    if (p->K >= 2 && das::bi_supported(p->B, cplx, p->bi_group, p->Q)) return DAS_KERNEL_BI;
+    if (p->K >= 2 && das::bi_supported(p->B, cplx, p->bi_group, p->Q, p->M, p->K)) return DAS_KERNEL_BI;
     return DAS_KERNEL_BL;
 }
 
@@ -151,11 +151,11 @@ das_status check_supported(const das_plan_s *p, int kernel)
     switch (kernel) {
     case DAS_KERNEL_BL: return DAS_OK;
     case DAS_KERNEL_BI:
-        if (p->K < 2 || !das::bi_supported(p->B, cplx, p->bi_group, p->Q))
+        if (p->K < 2 || !das::bi_supported(p->B, cplx, p->bi_group, p->Q, p->M, p->K))
             return fail(DAS_ERR_UNSUPPORTED,
-                        "BI kernel needs K >= 2, B a multiple of the group's 16-byte chunks and "
-                        "its transmit table in shared memory (B=%d, group=%d, Q=%d)", p->B,
-                        p->bi_group, p->Q);
+                        "BI kernel needs K >= 2, B a multiple of the group's 16-byte chunks, "
+                        "its transmit table in shared memory and a record of < 2^32 16-byte "
+                        "chunks (B=%d, group=%d, Q=%d)", p->B, p->bi_group, p->Q);
         return DAS_OK;
     case DAS_KERNEL_BRICK:
         if (!das::brick_supported(p->B, cplx, p->K, p->storage == DAS_STORAGE_F16))

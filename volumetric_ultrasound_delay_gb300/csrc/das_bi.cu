@@ -12,8 +12,9 @@
 // lane turns them into a row and two interpolation weights (IQ: and the
 // demodulation phase).  A ballot gives each group the receivers of the block
 // that contribute, and the group walks only those, U at a time, broadcasting
-// each receiver's row and weights from its lane and issuing the row loads of
-// the U receivers before their FMAs.  Real frames are accumulated in pairs
+// from each receiver's lane the 32-bit index (in 16-byte chunks) of its first
+// row and its two weights, and issuing the row loads of the U receivers
+// before their FMAs.  Real frames are accumulated in pairs
 // with the packed FP32 FMA (__ffma2_rn).
 #include "das_device.cuh"
 
@@ -40,7 +41,6 @@ das_bi_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__
     constexpr int NW = 32 / G;                    // voxels per warp
     constexpr int CH = CPLX ? 2 : 4;              // elements per 16-byte chunk
     constexpr int U = walk_step<CPLX>();
-    using T = typename std::conditional<CPLX, float2, float>::type;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int grp = lane / G;
@@ -51,7 +51,9 @@ das_bi_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__
     const float3 p = nvalid ? voxel_position(g, s) : make_float3(0.f, 0.f, 0.f);
     const int n = nvalid ? voxel_index(g, s) : 0;
     const long long qmb = (long long)g.Q * g.M * g.B;        // row stride of k
-    const T *permT = reinterpret_cast<const T *>(perm) + t * CH;
+    const float4 *perm4 = reinterpret_cast<const float4 *>(perm) + t;   // chunk t of a row
+    const long long qmbc = qmb / CH;                                    // row stride in chunks
+    const long long bc = g.B / CH;                                      // chunks per (q, m) row
 
     // per-voxel transmit delay (samples) and weight, once per CTA
     extern __shared__ float2 txs[];     // [THREADS / 32 * NW][Q]
@@ -92,10 +94,10 @@ das_bi_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__
                 ok = sample_pair(f, wq, g.K, r0, w0, w1);
                 if (CPLX && ok) ph = demod_phase(g, f);
             }
+            // chunk index of the first row of this lane's pair
+            const unsigned cidx = ok ? (unsigned)((long long)r0 * qmbc + ((long long)q * g.M + m) * bc) : 0u;
             // the group's contributing receivers of the block (same for all its lanes)
             unsigned mine = __ballot_sync(0xffffffffu, ok) & gmask;
-            // element offset of row k = 0 of slab (q, m0 + j) is slab + (grp * G + j) * B
-            const long long slab = ((long long)q * g.M + m0 - grp * G) * g.B;
             while (mine) {
                 // the next U receivers of the list (the lanes holding their values)
                 int src[U];
@@ -113,7 +115,7 @@ das_bi_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__
                 float2 W0[U], W1[U];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    const int rj = __shfl_sync(gmask, r0, src[u]);
+                    const unsigned cj = __shfl_sync(gmask, cidx, src[u]);
                     const float a0 = __shfl_sync(gmask, w0, src[u]);
                     const float a1 = __shfl_sync(gmask, w1, src[u]);
                     float2 pj = make_float2(1.f, 0.f);
@@ -123,14 +125,14 @@ das_bi_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__
                     }
                     W0[u] = CPLX ? make_float2(a0 * pj.x, a0 * pj.y) : make_float2(a0, a0);
                     W1[u] = CPLX ? make_float2(a1 * pj.x, a1 * pj.y) : make_float2(a1, a1);
-                    const T *p0 = permT + (slab + (long long)rj * qmb + (long long)src[u] * g.B);
+                    const float4 *p0 = perm4 + cj;
 #pragma unroll
                     for (int c = 0; c < J; ++c) {
                         v0[u][c] = make_float4(0.f, 0.f, 0.f, 0.f);
                         v1[u][c] = v0[u][c];
                         if (use[u]) {
-                            v0[u][c] = __ldg(reinterpret_cast<const float4 *>(p0 + c * G * CH));
-                            v1[u][c] = __ldg(reinterpret_cast<const float4 *>(p0 + qmb + c * G * CH));
+                            v0[u][c] = __ldg(p0 + c * G);
+                            v1[u][c] = __ldg(p0 + qmbc + c * G);
                         }
                     }
                 }
@@ -213,17 +215,20 @@ bool choose(int B, bool cplx, int group, int &G, int &J)
 
 }  // namespace
 
-bool bi_supported(int B, bool cplx, int group, int Q)
+bool bi_supported(int B, bool cplx, int group, int Q, int M, int K)
 {
     int G, J;
-    return choose(B, cplx, group, G, J) && smem_bytes(G, Q) <= SMEM_MAX;
+    // row indices travel as 32-bit counts of 16-byte chunks
+    const long long chunks = (long long)K * Q * M * B / (cplx ? 2 : 4);
+    return choose(B, cplx, group, G, J) && smem_bytes(G, Q) <= SMEM_MAX && chunks < (1LL << 32);
 }
 
 cudaError_t launch_bi(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
                       const float *w, void *out, bool cplx, int group, cudaStream_t stream)
 {
     int G, J;
-    if (!choose(g.B, cplx, group, G, J)) return cudaErrorInvalidValue;
+    if (!bi_supported(g.B, cplx, group, g.Q, g.M, g.K) || !choose(g.B, cplx, group, G, J))
+        return cudaErrorInvalidValue;
 #define DAS_BI_CASE(GG, JJ)                                                                     \
     if (G == GG && J == JJ)                                                                     \
         return cplx ? launch_one<GG, JJ, true>(g, rx, perm, tau, w, out, stream)                \

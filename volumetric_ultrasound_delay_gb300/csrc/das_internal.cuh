@@ -59,7 +59,7 @@ cudaError_t launch_bl(const DasGeom &g, const RxPos *rx, const void *rf, const f
                       const float *w, void *out, bool cplx, cudaStream_t stream);
 cudaError_t launch_bl64(const DasGeom64 &g, const Pos64 *rx, const void *rf, const float *tau,
                         const float *w, void *out, bool cplx, cudaStream_t stream);
-bool bi_supported(int B, bool cplx, int group, int Q);
+bool bi_supported(int B, bool cplx, int group, int Q, int M, int K);
 cudaError_t launch_bi(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
                       const float *w, void *out, bool cplx, int group, cudaStream_t stream);
 bool brick_supported(int B, bool cplx, int K, bool half = false);
