@@ -26,6 +26,11 @@ namespace das {
 namespace {
 
 constexpr int THREADS = 64;     // 2 warps per CTA
+// resident CTAs per SM the register allocation must allow: 24 (48 warps, 40
+// registers, a few bytes of spill) against 21 at the unconstrained 46
+// registers: 32 x 32-array volume 20.1 -> 18.6 ms; 28 or 32 CTAs spill more
+// and run 21 ms
+constexpr int MIN_BLOCKS = 24;
 
 // receivers per walk step: 2 for real data (32-frame float32 volume: 1 step
 // 30.0 ms, 2 21.7 ms, 4 28.9 ms); 1 for IQ, whose rows of 64 complex frames
@@ -34,7 +39,7 @@ template <bool CPLX>
 constexpr int walk_step() { return CPLX ? 1 : DAS_BI_U; }
 
 template <int G, int J, bool CPLX>
-__global__ void __launch_bounds__(THREADS)
+__global__ void __launch_bounds__(THREADS, MIN_BLOCKS)
 das_bi_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__ perm,
               const float *__restrict__ tau, const float *__restrict__ wtx, float *__restrict__ out)
 {
