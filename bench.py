@@ -20,7 +20,9 @@ Prints ONE JSON line (rank 0).  Besides the device-timed value it reports:
   cpu_baseline  the float64 oracle on the host cores, on a bounded voxel sample;
   e2e           the same metric through das_beamform_host with pinned host
                 buffers (host->device and device->host copies inside the timing);
-  clocks        SM clocks and throttle reasons sampled during the timed region.
+  clocks        SM clocks and throttle reasons sampled during the timed region;
+  pipeline      volumes alternating between two plans on two streams (the
+                permute of one overlaps the DAS kernel of the other), per volume.
 
 ``--impl reference`` times the oracle itself (the reference arm: a plain CPU
 program) on bounded samples of the same workload.  Under torchrun with N > 1
@@ -67,6 +69,10 @@ def parse_args():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--pipeline", type=int, default=20, metavar="V",
+                    help="also time V volumes alternating between two plans on two streams "
+                         "(the permute of one volume can overlap the DAS kernel of the other); "
+                         "0 = off; skipped for records that fit in L2")
     ap.add_argument("--n-el", type=int, default=None, help="override: array elements per side")
     ap.add_argument("--grid", type=int, nargs=3, default=None, metavar=("NX", "NY", "NZ"),
                     help="override: voxel grid (for small profiling cases)")
@@ -370,6 +376,37 @@ def run_ours(args, world, rank, local):
         if float((out_h - ref).abs().max()) > 1e-5 * float(ref.abs().max()):
             raise RuntimeError("host entry point disagrees with the device entry point")
 
+    # ---------------- two plans on two streams, volumes alternating (optional)
+    pipeline = None
+    if args.pipeline > 0 and not flush:
+        plan2 = das.Plan(prob.grid, prob.rx, prob.c, prob.fs, prob.t0, prob.fnum, dtype, prob.B,
+                         prob.Q, prob.M, prob.K, kernel=args.kernel, f_demod=prob.f_demod,
+                         storage=args.storage)
+        streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+        outs = [out, torch.empty_like(out)]
+        plans = [plan, plan2]
+        plan.set_option(das.OPT_TIMING, 0)
+        for i in range(4):                               # warm-up of both plans
+            plans[i % 2].beamform(rf, tau, w, outs[i % 2], stream=streams[i % 2])
+        torch.cuda.synchronize(dev)
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        joined = torch.cuda.Event()
+        start.record(streams[0])
+        streams[1].wait_event(start)
+        for i in range(args.pipeline):
+            plans[i % 2].beamform(rf, tau, w, outs[i % 2], stream=streams[i % 2])
+        joined.record(streams[1])
+        streams[0].wait_event(joined)
+        stop.record(streams[0])
+        torch.cuda.synchronize(dev)
+        p_ms = max_over_ranks(world, start.elapsed_time(stop)) / args.pipeline
+        pipeline = {"volumes": args.pipeline, "ms_per_volume": p_ms, "value": world * A / (p_ms / 1e3),
+                    "unit": UNIT, "plans": 2, "streams": 2,
+                    "vs_one_stream": ms_per_step / p_ms}
+        plan2.close()
+        plan.set_option(das.OPT_TIMING, 1)
+
     # ---------------- roofline of the dominant kernel (the DAS kernel)
     pairs = aperture_pairs(prob)
     a_eff = prob.B * prob.Q * pairs
@@ -447,6 +484,8 @@ def run_ours(args, world, rank, local):
         "gpu_launches": launches,
         "kernel_ms": {"permute": statistics.mean(perm_ms), "das": das_mean},
     }
+    if pipeline is not None:
+        line["pipeline"] = pipeline
     print(json.dumps(line), flush=True)
 
 
