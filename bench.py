@@ -101,8 +101,11 @@ def describe(wl) -> str:
 
 
 def aperture_pairs(prob) -> int:
-    """Number of (voxel, receiver) pairs inside the F-number aperture."""
+    """Number of (voxel, receiver) pairs inside the F-number aperture (all
+    pairs when F# <= 0 switches the aperture off)."""
     nx, ny, nz, x0, y0, z0, dx, dy, dz = prob.grid
+    if prob.fnum <= 0:
+        return nx * ny * nz * len(prob.rx)
     xs = x0 + np.arange(nx) * dx
     ys = y0 + np.arange(ny) * dy
     rx = prob.rx.astype(np.float64)
