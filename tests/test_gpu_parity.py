@@ -312,6 +312,44 @@ def test_host_entry_point_matches_device(oracle, small_problems, name, kernel, g
     assert np.abs(y - y_dev).max() <= 1e-5 * np.abs(y_dev).max()
 
 
+def test_host_entry_point_from_two_threads(small_problems):
+    """Two plans, each driven by its own host thread through the host entry
+    point on its own stream (what bench.py times as e2e.two_threads): every
+    call of either thread gives the single-threaded result."""
+    import threading
+    from volumetric_ultrasound_delay_gb300 import das
+    prob = small_problems["full_s"]
+    y_dev, _ = gpu_beamform(prob, "auto")
+    rf = torch.from_numpy(np.ascontiguousarray(prob.rf)).pin_memory()
+    tau = torch.from_numpy(prob.tau_tx).pin_memory()
+    w = torch.from_numpy(prob.w_tx).pin_memory()
+    plans = [plan_for(prob), plan_for(prob)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    results, errors = [[], []], []
+
+    def drive(i):
+        try:
+            out = torch.empty((prob.B, prob.N), dtype=torch.float32).pin_memory()
+            for _ in range(4):
+                plans[i].beamform_host(rf, tau, w, out, stream=streams[i])
+                results[i].append(out.numpy().copy())
+        except Exception as exc:
+            errors.append(exc)
+
+    threads = [threading.Thread(target=drive, args=(i,)) for i in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    for p in plans:
+        p.close()
+    assert not errors, errors
+    for ys in results:
+        assert len(ys) == 4
+        for y in ys:
+            assert np.abs(y - y_dev).max() <= 1e-5 * np.abs(y_dev).max()
+
+
 def test_two_plans_pipeline_volumes_on_two_streams(small_problems):
     """Successive volumes alternate between two plans on two streams (the
     permute of one volume can run beside the DAS kernel of the previous one);
