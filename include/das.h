@@ -209,7 +209,10 @@ das_status das_beamform(das_plan plan, const void *rf, const float *tau_tx,
  * copy stream, so the copy of one group overlaps the permute and sum of the
  * previous one; the other kernels copy everything, then run das_beamform.
  * Device buffers (about the size of rf) and the copy stream are created on first
- * use and kept.  Page-locked host memory is needed for the overlap.
+ * use and kept.  Page-locked host memory is needed for the overlap.  Different
+ * plans may be driven from different host threads at once (each call blocks
+ * only its own thread), which overlaps one volume's upload with another's
+ * kernels; one plan serves one call at a time.
  * Errors: as das_beamform.  Synchronous.
  */
 das_status das_beamform_host(das_plan plan, const void *rf_host, const float *tau_tx_host,
