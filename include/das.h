@@ -149,6 +149,8 @@ typedef struct {
  *            Q*M*(K+3) and B*N must stay below 2^31, K below 2^22.
  * Allocates the device copies of the geometry; the permute scratch of the BI,
  * brick and window kernels (B*Q*M*(K+3) elements) is allocated on first use.
+ * A plan's device memory comes from CUDA's stream-ordered allocator (the
+ * device's default memory pool) on a stream the plan owns.
  * Errors: DAS_ERR_INVALID_ARG, DAS_ERR_OUT_OF_MEMORY, DAS_ERR_CUDA; *plan is
  * set to NULL on failure.  The plan belongs to the device current at creation.
  */
@@ -174,8 +176,14 @@ das_status das_plan_create_points(das_plan *plan, const float *voxel_xyz, int N,
                                   const float *rx_xyz, float c, float fs, float t0, float fnum,
                                   das_dtype dtype, int B, int Q, int M, int K);
 
-/* Sets / reads one das_option.  Errors: DAS_ERR_INVALID_ARG (null plan, unknown
- * option or value), DAS_ERR_UNSUPPORTED (see DAS_OPT_DEMOD_HZ). */
+/* Sets / reads one das_option.  No passage of the pages defines this call: it
+ * is library plumbing that selects among the pages' kernels (BL, BI) and this
+ * library's own, and carries the IQ demodulation frequency of the IQ form of
+ * the sum (ffdas docs, "How It Works", "Mixed-precision storage": complex
+ * records) and the FP16 storage switch (ffdas paper, Methods, FP16
+ * paragraphs).  Takes effect from the next das_beamform; host only, no device
+ * work.  Errors: DAS_ERR_INVALID_ARG (null plan, unknown option or value),
+ * DAS_ERR_UNSUPPORTED (see DAS_OPT_DEMOD_HZ). */
 das_status das_plan_set_option(das_plan plan, int option, double value);
 das_status das_plan_get_option(das_plan plan, int option, double *value);
 
@@ -227,8 +235,14 @@ das_status das_plan_last_times(das_plan plan, float *permute_ms, float *das_ms);
 /* Bytes of device memory the plan holds now. */
 das_status das_plan_device_bytes(das_plan plan, size_t *bytes);
 
-/* Frees everything the plan owns (synchronous; waits for its device work).
- * A NULL plan is a no-op returning DAS_OK. */
+/* Frees everything the plan owns.  No passage of the pages defines this call:
+ * it is library plumbing that ends the life of a plan.
+ * It does not wait on the host, neither for this plan's queued work nor for
+ * any other stream: the plan's device memory is released in stream order, on
+ * the plan's own stream, after the last work that a das_beamform or
+ * das_beamform_host of this plan queued on the caller's stream, which still
+ * runs to completion and writes its output.  The plan handle is invalid once
+ * the call returns.  A NULL plan is a no-op returning DAS_OK. */
 das_status das_plan_destroy(das_plan plan);
 
 /*
@@ -290,9 +304,14 @@ das_status das_permute_bqmk_to_kqmb(const void *in, void *out, das_dtype dtype, 
  * overlaps (unordered streams, or several host threads) race on the array and
  * give wrong results, so serialise them.
  *
- * The first call on each device looks up the array's device address (with
- * that device current) before launching; make that first call before any
- * stream capture.
+ * Each call looks up the array's device address on the current device
+ * (cudaGetSymbolAddress, which allocates nothing), so a cudaDeviceReset or
+ * another context of the device between calls is harmless.  The first call on
+ * each device also loads libdas's kernels there; make that first call before
+ * any stream capture.
+ *
+ * rx_xyz is device memory, so its values are not checked on the host: a
+ * non-finite receiver position gives non-finite output rather than an error.
  *
  * Errors: DAS_ERR_INVALID_ARG (NULL or misaligned pointers, bad sizes, scratch
  * too small), DAS_ERR_UNSUPPORTED (B / K the brick kernel cannot serve,
@@ -304,7 +323,9 @@ das_status das_beamform_noalloc(const das_grid *grid, const float *rx_xyz, float
                                 const float *tau_tx, const float *w_tx, void *out,
                                 cudaStream_t stream);
 
-/* Text of the last error raised on the calling thread ("" if none). */
+/* Text of the last error raised on the calling thread ("" if none): a
+ * thread-local buffer owned by the library, valid until the thread's next libdas
+ * call.  No passage of the pages defines this call: it is library plumbing. */
 const char *das_last_error_string(void);
 
 /* Library version, e.g. "1.0.0". */

@@ -53,6 +53,11 @@ struct das_plan_s {
     bool timed_once = false;
     bool last_had_permute = false;
     cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+    // the plan's own stream (allocations, uploads, stream-ordered frees) and the
+    // event recorded after the last work each call queued on the caller's stream
+    cudaStream_t own = nullptr;
+    cudaEvent_t done = nullptr;
+    bool used = false;
     RxPos *d_rx = nullptr;
     float4 *d_vox = nullptr;                  // voxel list (sample units, slot order), list plans only
     int *d_order = nullptr;                   // list plans: caller's index of each slot
@@ -174,24 +179,67 @@ das_status check_supported(const das_plan_s *p, int kernel)
     }
 }
 
+// Device memory of a plan comes from the stream-ordered allocator on the
+// plan's own stream; once these return it is ready for use on any stream.
+template <typename T>
+cudaError_t plan_alloc(das_plan_s *p, T **ptr, size_t bytes)
+{
+    void *v = nullptr;
+    cudaError_t e = cudaMallocAsync(&v, bytes, p->own);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(p->own);
+    if (e != cudaSuccess) {
+        if (v) cudaFreeAsync(v, p->own);
+        v = nullptr;
+        cudaGetLastError();
+    }
+    *ptr = static_cast<T *>(v);
+    return e;
+}
+
+template <typename T>
+cudaError_t plan_upload(das_plan_s *p, T **ptr, const void *src, size_t bytes)
+{
+    cudaError_t e = plan_alloc(p, ptr, bytes);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(*ptr, src, bytes, cudaMemcpyHostToDevice, p->own);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(p->own);
+    return e;
+}
+
+// Releases everything the plan owns without waiting on the host: the device
+// buffers are freed on the plan's own stream after the event that marks the
+// end of the plan's last queued work, so neither this plan's queued work nor
+// any other stream is waited for; events and streams with work still pending
+// are released by CUDA once that work completes.
 void release(das_plan_s *p)
 {
-    cudaFree(p->d_rx);
-    cudaFree(p->d_vox);
-    cudaFree(p->d_order);
-    cudaFree(p->d_rx64);
-    cudaFree(p->d_vox64);
-    cudaFree(p->d_perm);
-    cudaFree(p->d_rf);
-    cudaFree(p->d_out);
-    cudaFree(p->d_tau);
-    cudaFree(p->d_w);
+    if (p->own) {
+        if (p->used && p->done) cudaStreamWaitEvent(p->own, p->done, 0);
+        void *bufs[] = {p->d_rx, p->d_vox, p->d_order, p->d_rx64, p->d_vox64,
+                        p->d_perm, p->d_rf, p->d_out, p->d_tau, p->d_w};
+        for (void *b : bufs)
+            if (b) cudaFreeAsync(b, p->own);
+    }
     for (auto &e : p->ev)
         if (e) cudaEventDestroy(e);
     for (auto &e : p->copy_ev)
         if (e) cudaEventDestroy(e);
+    if (p->done) cudaEventDestroy(p->done);
     if (p->copy_stream) cudaStreamDestroy(p->copy_stream);
+    if (p->own) cudaStreamDestroy(p->own);
+    cudaGetLastError();
 }
+
+// Records the plan's done event on the caller's stream when a call returns,
+// by whatever path, after it may have queued work there.
+struct DoneMark {
+    das_plan_s *p;
+    cudaStream_t stream;
+    ~DoneMark()
+    {
+        if (cudaEventRecord(p->done, stream) == cudaSuccess) p->used = true;
+        else cudaGetLastError();
+    }
+};
 
 // Allocates the permute scratch on first use (sized for the padded layout, the
 // larger one) and zeroes it when the padded layout is about to be used after
@@ -199,12 +247,8 @@ void release(das_plan_s *p)
 das_status ensure_scratch(das_plan_s *p, int layout, cudaStream_t stream)
 {
     if (!p->d_perm) {
-        cudaError_t e = cudaMalloc(&p->d_perm, p->padded_bytes());
-        if (e != cudaSuccess) {
-            p->d_perm = nullptr;
-            cudaGetLastError();
-            return cuda_fail(e, "permute scratch allocation");
-        }
+        cudaError_t e = plan_alloc(p, &p->d_perm, p->padded_bytes());
+        if (e != cudaSuccess) return cuda_fail(e, "permute scratch allocation");
         p->perm_bytes = p->padded_bytes();
         p->perm_pads_zero = false;
     }
@@ -286,6 +330,15 @@ das_status das_plan_create(das_plan *plan, const das_grid *grid, const float *rx
     if (e != cudaSuccess) { delete p; return cuda_fail(e, "cudaGetDevice"); }
     e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
     if (e != cudaSuccess) { delete p; return cuda_fail(e, "cudaDeviceGetAttribute"); }
+    e = cudaStreamCreateWithFlags(&p->own, cudaStreamNonBlocking);
+    if (e != cudaSuccess) { p->own = nullptr; delete p; return cuda_fail(e, "plan stream"); }
+    e = cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        p->done = nullptr;
+        release(p);
+        delete p;
+        return cuda_fail(e, "plan event");
+    }
 
     // positions in sample units (metres * fs / c), scaled in double
     const double s = (double)fs / (double)c;
@@ -317,14 +370,12 @@ das_status das_plan_create(das_plan *plan, const das_grid *grid, const float *rx
     g64.B = B; g64.Q = Q; g64.M = M; g64.K = K;
     g64.vox = nullptr;
 
-    e = cudaMalloc(&p->d_rx, sizeof(RxPos) * M);
-    if (e == cudaSuccess) e = cudaMemcpy(p->d_rx, hrx.data(), sizeof(RxPos) * M, cudaMemcpyHostToDevice);
+    e = plan_upload(p, &p->d_rx, hrx.data(), sizeof(RxPos) * M);
     if (e == cudaSuccess && p->is_double()) {
         std::vector<Pos64> h64(M);
         for (int m = 0; m < M; ++m)
             h64[m] = Pos64{rx_xyz[3 * m] * s, rx_xyz[3 * m + 1] * s, rx_xyz[3 * m + 2] * s, 0.0};
-        e = cudaMalloc(&p->d_rx64, sizeof(Pos64) * M);
-        if (e == cudaSuccess) e = cudaMemcpy(p->d_rx64, h64.data(), sizeof(Pos64) * M, cudaMemcpyHostToDevice);
+        e = plan_upload(p, &p->d_rx64, h64.data(), sizeof(Pos64) * M);
     }
     if (e != cudaSuccess) {
         release(p);
@@ -362,13 +413,12 @@ das_status das_plan_create_points(das_plan *plan, const float *voxel_xyz, int N,
         const float *v = voxel_xyz + 3 * (size_t)index(k);
         hv[k] = make_float4((float)(v[0] * s), (float)(v[1] * s), (float)(v[2] * s), 0.f);
     }
-    cudaError_t e = cudaMalloc(&p->d_vox, sizeof(float4) * (size_t)N);
-    if (e == cudaSuccess)
-        e = cudaMemcpy(p->d_vox, hv.data(), sizeof(float4) * (size_t)N, cudaMemcpyHostToDevice);
-    if (e == cudaSuccess && !order.empty()) {
-        e = cudaMalloc(&p->d_order, sizeof(int) * (size_t)N);
-        if (e == cudaSuccess)
-            e = cudaMemcpy(p->d_order, order.data(), sizeof(int) * (size_t)N, cudaMemcpyHostToDevice);
+    cudaError_t e;
+    {
+        DeviceGuard dg(p->device);
+        e = plan_upload(p, &p->d_vox, hv.data(), sizeof(float4) * (size_t)N);
+        if (e == cudaSuccess && !order.empty())
+            e = plan_upload(p, &p->d_order, order.data(), sizeof(int) * (size_t)N);
     }
     if (e != cudaSuccess) {
         das_plan_destroy(p);
@@ -385,9 +435,10 @@ das_status das_plan_create_points(das_plan *plan, const float *voxel_xyz, int N,
             const float *v = voxel_xyz + 3 * (size_t)index(k);
             h64[k] = Pos64{v[0] * s, v[1] * s, v[2] * s, 0.0};
         }
-        e = cudaMalloc(&p->d_vox64, sizeof(Pos64) * (size_t)N);
-        if (e == cudaSuccess)
-            e = cudaMemcpy(p->d_vox64, h64.data(), sizeof(Pos64) * (size_t)N, cudaMemcpyHostToDevice);
+        {
+            DeviceGuard dg(p->device);
+            e = plan_upload(p, &p->d_vox64, h64.data(), sizeof(Pos64) * (size_t)N);
+        }
         if (e != cudaSuccess) {
             das_plan_destroy(p);
             *plan = nullptr;
@@ -491,6 +542,7 @@ das_status das_beamform(das_plan p, const void *rf, const float *tau_tx, const f
     das_status st = check_supported(p, kernel);
     if (st != DAS_OK) return st;
     DeviceGuard dg(p->device);
+    DoneMark mark{p, stream};
     const bool cplx = p->is_complex();
 
     const void *src = rf;
@@ -545,14 +597,12 @@ das_status das_beamform_host(das_plan p, const void *rf_host, const float *tau_t
     if (st != DAS_OK) return st;
     DeviceGuard dg(p->device);
     cudaError_t e = cudaSuccess;
-    if (!p->d_rf) e = cudaMalloc(&p->d_rf, p->rf_bytes());
-    if (e == cudaSuccess && !p->d_out) e = cudaMalloc(&p->d_out, p->out_bytes());
-    if (e == cudaSuccess && !p->d_tau) e = cudaMalloc(&p->d_tau, p->txw_bytes());
-    if (e == cudaSuccess && !p->d_w) e = cudaMalloc(&p->d_w, p->txw_bytes());
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return cuda_fail(e, "host-path device buffers");
-    }
+    if (!p->d_rf) e = plan_alloc(p, &p->d_rf, p->rf_bytes());
+    if (e == cudaSuccess && !p->d_out) e = plan_alloc(p, &p->d_out, p->out_bytes());
+    if (e == cudaSuccess && !p->d_tau) e = plan_alloc(p, &p->d_tau, p->txw_bytes());
+    if (e == cudaSuccess && !p->d_w) e = plan_alloc(p, &p->d_w, p->txw_bytes());
+    if (e != cudaSuccess) return cuda_fail(e, "host-path device buffers");
+    DoneMark mark{p, stream};
     int groups = p->host_groups > 0 ? p->host_groups : (p->Q < 5 ? p->Q : 5);
     if (kernel != DAS_KERNEL_BRICK && kernel != DAS_KERNEL_WINDOW)
         groups = 1;                                  // only these kernels sum transmit ranges
@@ -654,7 +704,6 @@ das_status das_plan_destroy(das_plan p)
     if (!p) return DAS_OK;
     {
         DeviceGuard dg(p->device);
-        cudaDeviceSynchronize();
         release(p);
     }
     delete p;

@@ -131,14 +131,14 @@ das_bi_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__
                     W0[u] = CPLX ? make_float2(a0 * pj.x, a0 * pj.y) : make_float2(a0, a0);
                     W1[u] = CPLX ? make_float2(a1 * pj.x, a1 * pj.y) : make_float2(a1, a1);
                     const float4 *p0 = perm4 + cj;
+                    // a row standing in for a sample outside the record is not read
+                    const bool r0_in = use[u] && !skip_row(a0), r1_in = use[u] && !skip_row(a1);
 #pragma unroll
                     for (int c = 0; c < J; ++c) {
                         v0[u][c] = make_float4(0.f, 0.f, 0.f, 0.f);
                         v1[u][c] = v0[u][c];
-                        if (use[u]) {
-                            v0[u][c] = __ldg(p0 + c * G);
-                            v1[u][c] = __ldg(p0 + qmbc + c * G);
-                        }
+                        if (r0_in) v0[u][c] = __ldg(p0 + c * G);
+                        if (r1_in) v1[u][c] = __ldg(p0 + qmbc + c * G);
                     }
                 }
 #pragma unroll

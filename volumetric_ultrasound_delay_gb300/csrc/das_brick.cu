@@ -80,17 +80,21 @@ struct BrickShape {
 };
 
 // Real entry: one 32-bit word, the row relative to the first row of the block
-// of receivers in the high bits and the interpolation fraction in the low FB
-// bits (FB >= 10; for K = 2048, 15 bits, a step of 3e-5 samples, 8x finer
-// than float32 resolves f near K) -- or {row, fraction} in float32 bits.
+// of receivers in the high bits and the interpolation fraction, rounded to
+// nearest (at most 1 - 2^-FB), in the low FB bits (FB >= 10; for K = 2048, 15 bits, a step of 3e-5
+// samples, 8x finer than float32 resolves f near K; for K = 65536, 10 bits, a
+// step of 1e-3 samples, half the float32 resolution of f there) -- or {row,
+// fraction} in float32 bits.
 // IQ entry: {row, fraction, cos, sin} in float32 bits.  Real entries are
 // packed for float32 storage, whose phase C is bound by shared-memory and L1
-// traffic; half storage moves half the bytes and keeps the undecoded floats.
-template <bool CPLX, bool HALF>
-constexpr bool packed_entries() { return !CPLX && !HALF && DAS_BRICK_PACKED != 0; }
-template <bool CPLX, bool HALF>
+// traffic, while at least MIN_PACKED_BITS fraction bits remain (K <= 8189);
+// longer records (WIDE) and half storage keep the undecoded floats.
+constexpr int MIN_PACKED_BITS = 14;
+template <bool CPLX, bool HALF, bool WIDE>
+constexpr bool packed_entries() { return !CPLX && !HALF && !WIDE && DAS_BRICK_PACKED != 0; }
+template <bool CPLX, bool HALF, bool WIDE>
 using Entry = typename std::conditional<CPLX, float4,
-                                        typename std::conditional<packed_entries<CPLX, HALF>(),
+                                        typename std::conditional<packed_entries<CPLX, HALF, WIDE>(),
                                                                   unsigned, float2>::type>::type;
 
 // entries per voxel list: MC plus padding, so that a list starts on a 16-byte
@@ -125,11 +129,11 @@ struct Layout {
     static constexpr int NP = CPLX ? EPC : EPC / 2;
 };
 
-template <int G, bool CPLX, bool HALF>
+template <int G, bool CPLX, bool HALF, bool WIDE>
 size_t smem_bytes(int Q)
 {
     constexpr int V = WARPS * (32 / G);
-    return sizeof(Entry<CPLX, HALF>) * 2 * V * entry_stride<CPLX>() + sizeof(float2) * (size_t)V * Q;
+    return sizeof(Entry<CPLX, HALF, WIDE>) * 2 * V * entry_stride<CPLX>() + sizeof(float2) * (size_t)V * Q;
 }
 
 // One pipelined trip of phase C: U entries, their fractions (and phases) and
@@ -222,7 +226,7 @@ constexpr int min_blocks()
 template <int J, bool HALF>
 constexpr int trip_size() { return J >= 4 ? 1 : (J == 2 ? 2 : DAS_BRICK_U1); }
 
-template <int G, int J, bool CPLX, bool HALF, bool SPLIT>
+template <int G, int J, bool CPLX, bool HALF, bool SPLIT, bool WIDE>
 __global__ void __launch_bounds__(THREADS, min_blocks<G, J, CPLX, HALF>())
 das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict__ perm,
                  const float *__restrict__ tau, const float *__restrict__ wtx,
@@ -241,8 +245,8 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
     constexpr int CPR = ROWB / 16;                 // 16-byte chunks per row
     constexpr int U = trip_size<J, HALF>();        // receivers per loop trip
     constexpr int ES = entry_stride<CPLX>();
-    using E = Entry<CPLX, HALF>;
-    constexpr bool PACKED = packed_entries<CPLX, HALF>();
+    using E = Entry<CPLX, HALF, WIDE>;
+    constexpr bool PACKED = packed_entries<CPLX, HALF, WIDE>();
 
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int tid = threadIdx.x;
@@ -351,7 +355,11 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                             const float2 ph = demod_phase(g, f);
                             e = make_float4(__int_as_float(base_row + rel), a, ph.x, ph.y);
                         } else if constexpr (PACKED) {
-                            e = ((unsigned)rel << fb) | __float2uint_rz(a * frac_scale);
+                            // fraction rounded to the nearest of its 2^fb steps, the
+                            // last step kept below 1 so the entry still reads rows
+                            // k0 and k0 + 1, the two samples the sum multiplies
+                            e = ((unsigned)rel << fb) |
+                                min(__float2uint_rn(a * frac_scale), frac_mask);
                         } else {
                             e = make_float2(__int_as_float(base_row + rel), a);
                         }
@@ -485,7 +493,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
         }
 }
 
-template <int G, int J, bool CPLX, bool HALF, bool SPLIT>
+template <int G, int J, bool CPLX, bool HALF, bool SPLIT, bool WIDE>
 cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
                        const float *w, void *out, cudaStream_t stream, int q0, int q1, bool acc)
 {
@@ -496,8 +504,8 @@ cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, cons
     const int bricks_y = g.vox ? 1 : (g.ny + BY - 1) / BY;
     const long long blocks = (long long)bricks_x * bricks_y * (g.vox ? 1 : g.nz);
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    const size_t smem = smem_bytes<G, CPLX, HALF>(g.Q);
-    auto kernel = das_brick_kernel<G, J, CPLX, HALF, SPLIT>;
+    const size_t smem = smem_bytes<G, CPLX, HALF, WIDE>(g.Q);
+    auto kernel = das_brick_kernel<G, J, CPLX, HALF, SPLIT, WIDE>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     kernel<<<(int)blocks, THREADS, smem, stream>>>(g, rx, perm, tau, w, static_cast<float *>(out),
@@ -552,7 +560,7 @@ bool brick_supported(int B, bool cplx, int K, bool half)
 {
     int G, J;
     bool split;
-    return K >= 2 && fraction_bits(K) >= 10 && choose(B, cplx, half, G, J, split);
+    return K >= 2 && choose(B, cplx, half, G, J, split);
 }
 
 cudaError_t launch_brick(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
@@ -564,17 +572,27 @@ cudaError_t launch_brick(const DasGeom &g, const RxPos *rx, const void *perm, co
     if (q1 < 0) q1 = g.Q;
     if (q0 < 0 || q0 > q1 || q1 > g.Q) return cudaErrorInvalidValue;
     if (g.K < 2 || !choose(g.B, cplx, half, G, J, split)) return cudaErrorInvalidValue;
+    // packed real entries while enough fraction bits remain, float entries beyond
+    const bool wide = fraction_bits(g.K) < MIN_PACKED_BITS;
+#define DAS_BRICK_ARGS g, rx, perm, tau, w, out, stream, q0, q1, accumulate
 #define DAS_BRICK_CASE(GG, JJ, HH, SS)                                                         \
     if (G == GG && J == JJ && half == HH && split == SS)                                       \
-        return cplx ? launch_one<GG, JJ, true, HH, SS>(g, rx, perm, tau, w, out, stream, q0, q1, accumulate) \
-                    : launch_one<GG, JJ, false, HH, SS>(g, rx, perm, tau, w, out, stream, q0, q1, accumulate);
-    DAS_BRICK_CASE(2, 1, false, false) DAS_BRICK_CASE(4, 1, false, false)
-    DAS_BRICK_CASE(8, 1, false, false) DAS_BRICK_CASE(8, 2, false, false)
-    DAS_BRICK_CASE(8, 4, false, false)
-    DAS_BRICK_CASE(16, 1, false, false) DAS_BRICK_CASE(16, 2, false, false)
+        return cplx ? launch_one<GG, JJ, true, HH, SS, false>(DAS_BRICK_ARGS)                  \
+                    : launch_one<GG, JJ, false, HH, SS, false>(DAS_BRICK_ARGS);
+#define DAS_BRICK_CASE_WIDE(GG, JJ)                                                            \
+    if (G == GG && J == JJ && !half && !split)                                                 \
+        return cplx ? launch_one<GG, JJ, true, false, false, false>(DAS_BRICK_ARGS)            \
+                    : (wide ? launch_one<GG, JJ, false, false, false, true>(DAS_BRICK_ARGS)    \
+                            : launch_one<GG, JJ, false, false, false, false>(DAS_BRICK_ARGS));
+    DAS_BRICK_CASE_WIDE(2, 1) DAS_BRICK_CASE_WIDE(4, 1)
+    DAS_BRICK_CASE_WIDE(8, 1) DAS_BRICK_CASE_WIDE(8, 2)
+    DAS_BRICK_CASE_WIDE(8, 4)
+    DAS_BRICK_CASE_WIDE(16, 1) DAS_BRICK_CASE_WIDE(16, 2)
     DAS_BRICK_CASE(2, 1, true, true) DAS_BRICK_CASE(4, 1, true, true) DAS_BRICK_CASE(8, 1, true, true)
     DAS_BRICK_CASE(8, 1, true, false) DAS_BRICK_CASE(8, 2, true, false)
 #undef DAS_BRICK_CASE
+#undef DAS_BRICK_CASE_WIDE
+#undef DAS_BRICK_ARGS
     return cudaErrorInvalidValue;
 }
 

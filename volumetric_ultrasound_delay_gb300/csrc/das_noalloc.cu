@@ -12,10 +12,11 @@
 // The scratch is a file-scope __device__ array of DAS_NOALLOC_SCRATCH_BYTES
 // (64 MiB).  Every GPU on which libdas's kernels are loaded holds it until the
 // process exits.  Host code may not use the array's name as an address (on the
-// host it is only a stand-in), so set-up looks up its device address with
-// cudaGetSymbolAddress, once per device with that device current, and passes
-// that pointer to the kernels.
-#include <atomic>
+// host it is only a stand-in), so each call looks up its device address with
+// cudaGetSymbolAddress, with the caller's device current, and passes that
+// pointer to the kernels.  The lookup allocates nothing and is repeated on
+// every call rather than cached: after a cudaDeviceReset, or under another
+// context of the same device, the array lives at a different address.
 #include <cmath>
 #include <cstdio>
 
@@ -27,9 +28,6 @@ namespace {
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[DAS_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::atomic<void *> g_scratch_addr[kMaxDevices];
-
 das_status reject(das_status st, const char *msg)
 {
     char text[320];
@@ -38,13 +36,15 @@ das_status reject(das_status st, const char *msg)
     return st;
 }
 
-// receiver positions (metres, M x 3) -> sample units in the scratch array
+// receiver positions (metres, M x 3) -> sample units in the scratch array,
+// scaled in double and rounded once to float, as a plan scales them on the host
 __global__ void scale_receivers(const float *__restrict__ rx_xyz, RxPos *__restrict__ dst, int M,
-                                float s)
+                                double s)
 {
     const int m = blockIdx.x * blockDim.x + threadIdx.x;
     if (m < M)
-        dst[m] = make_float4(rx_xyz[3 * m] * s, rx_xyz[3 * m + 1] * s, rx_xyz[3 * m + 2] * s, 0.f);
+        dst[m] = make_float4((float)((double)rx_xyz[3 * m] * s), (float)((double)rx_xyz[3 * m + 1] * s),
+                             (float)((double)rx_xyz[3 * m + 2] * s), 0.f);
 }
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -67,6 +67,9 @@ extern "C" das_status das_beamform_noalloc(const das_grid *grid, const float *rx
     if (!(c > 0.f) || !(fs > 0.f) || !std::isfinite(c) || !std::isfinite(fs) ||
         !std::isfinite(t0) || !std::isfinite(fnum) || !std::isfinite(f_demod))
         return reject(DAS_ERR_INVALID_ARG, "c and fs must be > 0; t0, fnum, f_demod finite");
+    const float gf[6] = {grid->x0, grid->y0, grid->z0, grid->dx, grid->dy, grid->dz};
+    for (float v : gf)
+        if (!std::isfinite(v)) return reject(DAS_ERR_INVALID_ARG, "grid origin/spacing not finite");
     if (dtype != DAS_F32 && dtype != DAS_C64) return reject(DAS_ERR_INVALID_ARG, "unknown dtype");
     if (dtype == DAS_F32 && f_demod != 0.0)
         return reject(DAS_ERR_UNSUPPORTED, "demodulation needs DAS_C64 data");
@@ -91,17 +94,15 @@ extern "C" das_status das_beamform_noalloc(const das_grid *grid, const float *rx
         (reinterpret_cast<uintptr_t>(w_tx) & 3u) || (reinterpret_cast<uintptr_t>(rx_xyz) & 3u))
         return reject(DAS_ERR_INVALID_ARG, "rf/out must be 16-byte and rx/tau/w 4-byte aligned");
 
-    // ---- set-up, once per device, with that device current
+    // ---- the scratch array's address on the current device (the first call on a
+    // device also loads the library's kernels there)
     int dev = 0, sms = 1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return reject(DAS_ERR_CUDA, cudaGetErrorString(e));
-    if (dev < 0 || dev >= kMaxDevices) return reject(DAS_ERR_UNSUPPORTED, "device index too large");
-    void *scratch = g_scratch_addr[dev].load(std::memory_order_acquire);
-    if (!scratch) {
-        e = cudaGetSymbolAddress(&scratch, g_noalloc_scratch);
-        if (e != cudaSuccess || !scratch) return reject(DAS_ERR_CUDA, cudaGetErrorString(e));
-        g_scratch_addr[dev].store(scratch, std::memory_order_release);
-    }
+    void *scratch = nullptr;
+    e = cudaGetSymbolAddress(&scratch, g_noalloc_scratch);
+    if (e != cudaSuccess || !scratch)
+        return reject(DAS_ERR_CUDA, e != cudaSuccess ? cudaGetErrorString(e) : "no scratch address");
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return reject(DAS_ERR_CUDA, cudaGetErrorString(e));
 
@@ -127,7 +128,7 @@ extern "C" das_status das_beamform_noalloc(const das_grid *grid, const float *rx
     // leave other data behind, so clear the region this call uses
     e = cudaMemsetAsync(perm, 0, perm_bytes, stream);
     if (e != cudaSuccess) return reject(DAS_ERR_CUDA, cudaGetErrorString(e));
-    scale_receivers<<<(M + 127) / 128, 128, 0, stream>>>(rx_xyz, rx_dev, M, (float)s);
+    scale_receivers<<<(M + 127) / 128, 128, 0, stream>>>(rx_xyz, rx_dev, M, s);
     e = cudaGetLastError();
     if (e == cudaSuccess) e = das::launch_permute(rf, perm, (int)elem, B, Q, M, K, 2, sms, stream);
     if (e == cudaSuccess) e = das::launch_brick(g, rx_dev, perm, tau_tx, w_tx, out, cplx, stream);
