@@ -65,7 +65,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="full", choices=["tiny", "mid", "full", "iq", "large"])
-    ap.add_argument("--kernel", default="auto", choices=["auto", "bl", "bi", "brick", "window"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "bl", "bi", "brick", "window", "pair"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
@@ -229,7 +229,8 @@ def max_over_ranks(world, value: float) -> float:
 
 
 def source_sha(kernel: str) -> str:
-    name = {"brick": "das_brick.cu", "window": "das_window.cu", "bi": "das_bi.cu", "bl": "das_bl.cu"}[kernel]
+    name = {"brick": "das_brick.cu", "window": "das_window.cu", "bi": "das_bi.cu", "bl": "das_bl.cu",
+            "pair": "das_pair.cu"}[kernel]
     h = hashlib.sha256()
     for f in (name, "das_device.cuh", "das_internal.cuh"):
         with open(os.path.join(ROOT, "volumetric_ultrasound_delay_gb300", "csrc", f), "rb") as fh:

@@ -80,7 +80,7 @@ typedef enum {
                               per-(voxel, transmit, receiver) geometry staged in
                               shared memory, receivers outside every aperture of
                               the brick skipped, zero-padded Q x M x (K+3) x B copy */
-    DAS_KERNEL_WINDOW = 4  /* this library's second sm_103a design on the same copy:
+    DAS_KERNEL_WINDOW = 4, /* this library's second sm_103a design on the same copy:
                               a group of lanes owns a 2 x 2 quad of voxels and loads
                               the window of rows the quad needs for a (transmit,
                               receiver) once, with one coefficient per voxel and row.
@@ -89,6 +89,13 @@ typedef enum {
                               row (zero weight times inf/NaN); on request
                               (AUTO keeps the brick kernel, faster on the workloads
                               measured so far) */
+    DAS_KERNEL_PAIR = 5    /* this library's third sm_103a design on the same copy: a
+                              group of lanes owns two neighbouring voxels and, per
+                              (transmit, receiver), loads the two or three rows their
+                              sample pairs span once, applying both voxels' weights to
+                              them; float32 records with B in {16, 32, 64}; exact for
+                              non-finite samples too (the permute flags them and the
+                              kernel then adds every term to its own voxel only) */
 } das_kernel;
 
 /* Plan options. */
@@ -113,8 +120,10 @@ typedef enum {
  * half precision in the permute and converts back to float32 before the
  * interpolation and the sum (ffdas paper, Methods, FP16 paragraphs; ffdas docs,
  * "Mixed-precision storage"): it halves the bytes the kernel reads, and y is
- * then DAS of the half-rounded record.  Served by the brick kernel only
- * (B * 2 bytes, complex B * 4, a multiple of 16); the other kernels return
+ * then DAS of the half-rounded record.  Served by the brick kernel (B * 2
+ * bytes, complex B * 4, a multiple of 16) and by the BI kernel (the pages'
+ * BI-FP16 variant, one 16-byte chunk per lane: B in {16, 32, 64, 128} for
+ * real records, {8, 16, 32, 64} for IQ); the other kernels return
  * DAS_ERR_UNSUPPORTED. */
 typedef enum {
     DAS_STORAGE_NATIVE = 0,

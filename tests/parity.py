@@ -13,6 +13,18 @@ DTYPE_NAMES = {np.dtype(np.float32): "f32", np.dtype(np.complex64): "c64",
                np.dtype(np.float64): "f64", np.dtype(np.complex128): "c128"}
 
 
+def kernel_serves(kernel, prob) -> bool:
+    """Whether a kernel with a restricted scope serves a problem's record: the
+    window kernel takes float32 records of 8, 16 or 32 frames, the pair kernel
+    float32 records of 16, 32 or 64 frames (the others serve, or reject, more
+    general shapes themselves)."""
+    if kernel == "window":
+        return prob.rf.dtype == np.float32 and prob.B in (8, 16, 32)
+    if kernel == "pair":
+        return prob.rf.dtype == np.float32 and prob.B in (16, 32, 64)
+    return True
+
+
 def plan_for(prob, kernel="auto"):
     from volumetric_ultrasound_delay_gb300 import das
     dtype = DTYPE_NAMES[prob.rf.dtype]

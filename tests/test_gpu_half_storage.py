@@ -1,8 +1,8 @@
 """Half-precision storage of the permuted record (DAS_STORAGE_F16).
 
 The permute rounds every float32 sample (complex: each component) to float16,
-and the brick kernel converts back to float32 before interpolating.  So the
-kernel computes DAS of the half-rounded record exactly as well as it computes
+and the brick and BI kernels convert back to float32 before interpolating.  So
+a kernel computes DAS of the half-rounded record exactly as well as it computes
 DAS of a float32 record: the oracle, fed that same rounded record, is held to
 the usual 1e-4-of-peak bar.  The rounding itself is checked bit for bit
 against numpy's float16 conversion (round to nearest even).
@@ -34,11 +34,11 @@ def half_rounded(prob):
     return rounded
 
 
-def run_half(prob, host=False, groups=0):
+def run_half(prob, host=False, groups=0, kernel="auto"):
     from volumetric_ultrasound_delay_gb300 import das
-    plan = plan_for(prob)
+    plan = plan_for(prob, kernel)
     plan.set_option(das.OPT_STORAGE, das.STORAGE_F16)
-    assert plan.kernel == "brick"
+    assert plan.kernel == ("brick" if kernel == "auto" else kernel)
     if host:
         plan.set_option(das.OPT_HOST_GROUPS, groups)
         out = np.empty((prob.B, prob.N), dtype=prob.rf.dtype)
@@ -82,11 +82,14 @@ SMALL = {
 }
 
 
+@pytest.mark.parametrize("kernel", ["auto", "bi"])
 @pytest.mark.parametrize("name", list(SMALL))
-def test_half_storage_matches_oracle_on_rounded_record(oracle, name):
+def test_half_storage_matches_oracle_on_rounded_record(oracle, name, kernel):
     kw = dict(SMALL[name])
     prob = synth.make_problem(kw.pop("base"), **kw)
-    y = run_half(prob)
+    if kernel == "bi" and name == "tiny":
+        pytest.skip("8 half frames fill one 16-byte chunk: BI needs two per voxel")
+    y = run_half(prob, kernel=kernel)
     ref, slack = oracle_beamform(oracle, half_rounded(prob))
     assert error_ratio(y, ref, slack) <= TOL
     # and it stays close to DAS of the float32 record (half rounding ~5e-4 per sample)
@@ -102,10 +105,11 @@ def test_half_storage_host_path_streams(oracle):
         assert error_ratio(y, ref, slack) <= TOL
 
 
-def test_half_storage_full_size_sampled(oracle):
+@pytest.mark.parametrize("kernel", ["auto", "bi"])
+def test_half_storage_full_size_sampled(oracle, kernel):
     prob = synth.make_problem("full")
     idx = synth.sample_voxels(prob.N, 512, seed=prob.wl.seed)
-    y = run_half(prob)
+    y = run_half(prob, kernel=kernel)
     ref, slack = oracle_beamform(oracle, half_rounded(prob), idx=idx)
     assert error_ratio(y[:, idx], ref, slack) <= TOL
 
@@ -118,8 +122,9 @@ def test_half_storage_rejections():
     with pytest.raises(das.DasError) as exc:
         plan.beamform(*device_inputs(prob))
     assert exc.value.status == das.DAS_ERR_UNSUPPORTED
-    plan.set_option(das.OPT_KERNEL, das.KERNELS["bi"])
-    with pytest.raises(das.DasError) as exc:
-        plan.beamform(*device_inputs(prob))
-    assert exc.value.status == das.DAS_ERR_UNSUPPORTED
+    for kernel in ("bi", "bl", "window", "pair"):
+        plan.set_option(das.OPT_KERNEL, das.KERNELS[kernel])
+        with pytest.raises(das.DasError) as exc:
+            plan.beamform(*device_inputs(prob))
+        assert exc.value.status == das.DAS_ERR_UNSUPPORTED
     plan.close()

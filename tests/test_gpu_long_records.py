@@ -11,7 +11,7 @@ entries for longer records, so the fraction is never coarser than float32
 size per term comes close to the parity bar).  Records are noise-free
 point-scatterer echoes
 (scatterers at voxel positions), a few frames, and small grids, so the oracle
-stays fast."""
+stays fast (16 frames, one transmit)."""
 import numpy as np
 import pytest
 
@@ -24,7 +24,7 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():  # pragma: no cover - CPU containers skip these
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
-KERNELS = ["bl", "bi", "brick", "window"]
+KERNELS = ["bl", "bi", "brick", "window", "pair"]
 
 CASES = {
     "K16384_shallow": dict(base="tiny", K=16384, fs=20e6, z_range=(5e-3, 20e-3)),
@@ -36,7 +36,8 @@ CASES = {
 def long_problem(name):
     kw = dict(CASES[name])
     base = kw.pop("base")
-    wl = synth.workload(base, nx=6, ny=6, nz=12, noise=False, n_scat=0, **kw)
+    wl = synth.workload(base, nx=6, ny=6, nz=12, B=16, angles_x_deg=(0.0,), noise=False, n_scat=0,
+                        **kw)
     prob = synth.make_problem(wl)
     pts = synth.grid_points(prob.grid)
     picks = np.linspace(0, prob.N - 1, 6).astype(int)[1:-1]

@@ -14,7 +14,7 @@ matches the oracle."""
 import numpy as np
 import pytest
 
-from parity import TOL, gpu_beamform, oracle_beamform
+from parity import TOL, gpu_beamform, kernel_serves, oracle_beamform
 from volumetric_ultrasound_delay_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -23,7 +23,7 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():  # pragma: no cover - CPU containers skip these
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
-EXACT = ["bl", "bi", "brick"]
+EXACT = ["bl", "bi", "brick", "pair"]
 
 
 def _index(prob, n, q, m):
@@ -88,6 +88,8 @@ def planted(request, oracle):
 @pytest.mark.parametrize("kernel", EXACT)
 def test_nonfinite_samples_match_oracle(planted, kernel):
     prob, ref, slack = planted
+    if not kernel_serves(kernel, prob):
+        pytest.skip(f"the {kernel} kernel does not serve this record")
     y, used = gpu_beamform(prob, kernel)
     assert used == kernel
     _compare(y, ref, slack)
@@ -116,13 +118,13 @@ def test_nan_beside_record_edge_stays_out(oracle, kernel, edge):
     """A pair straddling an end of the record keeps only its in-record sample:
     a NaN at the sample beyond that one (k = 1 at the start, k = K - 2 at the
     end) must not reach the output through a zero weight."""
-    base = synth.make_problem("tiny")
+    base = synth.make_problem("tiny", B=16)
     n, q, m = 16 * 16 * 8 + 16 * 8 + 8, 1, 27
     f = _index(base, n, q, m)
     # t0 shifted so that this term's index lands at -0.5 (pair k0 = -1) or K - 0.5
     target = -0.5 if edge == "start" else base.K - 0.5
     t0 = float(np.float32(base.t0 + (f - target) / base.fs))
-    prob = synth.make_problem("tiny", t0=t0)
+    prob = synth.make_problem("tiny", B=16, t0=t0)
     f = _index(prob, n, q, m)
     assert (-1 < f < 0) if edge == "start" else (prob.K - 1 < f < prob.K)
     k_nan = 1 if edge == "start" else prob.K - 2

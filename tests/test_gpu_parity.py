@@ -11,7 +11,7 @@ import zlib
 import numpy as np
 import pytest
 
-from parity import TOL, device_inputs, error_ratio, gpu_beamform, oracle_beamform, plan_for
+from parity import TOL, device_inputs, error_ratio, gpu_beamform, kernel_serves, oracle_beamform, plan_for
 from volumetric_ultrasound_delay_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -20,12 +20,8 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():  # pragma: no cover - CPU containers skip these
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
-KERNELS = ["bl", "bi", "brick", "window"]
-
-
-def window_serves(prob):
-    """The window kernel takes float32 records of 8, 16 or 32 frames."""
-    return prob.rf.dtype == np.float32 and prob.B in (8, 16, 32)
+KERNELS = ["bl", "bi", "brick", "window", "pair"]
+RESTRICTED = ("bi", "brick", "window", "pair")     # may reject a record shape
 
 # Workloads shrunk (8x8 array, small ragged grids) so the oracle finishes in a
 # second or two; B, Q, K, dtype and transmit geometry are those of each workload.
@@ -104,7 +100,7 @@ def test_batch_inner_permute_entry_point(oracle, dtype):
 def test_small_workload_all_voxels(oracle, small_problems, name, kernel):
     from volumetric_ultrasound_delay_gb300 import das
     prob = small_problems[name]
-    if kernel == "window" and not window_serves(prob):
+    if not kernel_serves(kernel, prob):
         with pytest.raises(das.DasError) as exc:
             gpu_beamform(prob, kernel)
         assert exc.value.status == das.DAS_ERR_UNSUPPORTED
@@ -120,7 +116,7 @@ def test_small_workload_all_voxels(oracle, small_problems, name, kernel):
                                        ("iq_s", "brick")])
 def test_auto_choice_and_kernels_agree(small_problems, name, auto):
     prob = small_problems[name]
-    kernels = [k for k in KERNELS if k != "window" or window_serves(prob)]
+    kernels = [k for k in KERNELS if kernel_serves(k, prob)]
     outs = {k: gpu_beamform(prob, k)[0] for k in kernels}
     y_auto, used = gpu_beamform(prob, "auto")
     assert used == auto
@@ -172,9 +168,8 @@ def test_edge_cases(oracle, name):
         try:
             y, _ = gpu_beamform(prob, kernel)
         except das.DasError as exc:
-            assert exc.status == das.DAS_ERR_UNSUPPORTED and kernel in ("bi", "brick", "window"), \
-                (name, kernel)
-            assert kernel != "window" or not window_serves(prob), name
+            assert exc.status == das.DAS_ERR_UNSUPPORTED and kernel in RESTRICTED, (name, kernel)
+            assert kernel not in ("window", "pair") or not kernel_serves(kernel, prob), (name, kernel)
             continue
         assert error_ratio(y, ref, slack) <= TOL, (name, kernel, error_ratio(y, ref, slack))
 
@@ -184,7 +179,7 @@ def test_nan_delay_contributes_nothing(oracle):
     prob.tau_tx[1, 3] = np.nan
     prob.tau_tx[0, 5] = np.inf
     ref, slack = oracle_beamform(oracle, prob)
-    for kernel in KERNELS:
+    for kernel in [k for k in KERNELS if kernel_serves(k, prob)]:
         y, _ = gpu_beamform(prob, kernel)
         assert np.all(np.isfinite(y)), kernel
         assert error_ratio(y, ref, slack) <= TOL, kernel
@@ -192,7 +187,7 @@ def test_nan_delay_contributes_nothing(oracle):
 
 def test_all_outside_aperture_is_zero():
     # voxels above the array (dz < 0): no receiver is inside any aperture
-    prob = _custom(z_range=(-4e-3, -2e-3))
+    prob = _custom(z_range=(-4e-3, -2e-3), B=16)
     for kernel in KERNELS:
         y, _ = gpu_beamform(prob, kernel)
         assert not np.any(y), kernel
@@ -201,7 +196,7 @@ def test_all_outside_aperture_is_zero():
 def test_unsupported_requests_are_rejected():
     from volumetric_ultrasound_delay_gb300 import das
     prob = _custom(B=3)
-    for kernel in ("bi", "brick", "window"):
+    for kernel in RESTRICTED:
         with pytest.raises(das.DasError) as exc:
             gpu_beamform(prob, kernel)
         assert exc.value.status == das.DAS_ERR_UNSUPPORTED
@@ -286,7 +281,8 @@ def test_misaligned_and_wrong_sizes_rejected():
 
 @pytest.mark.parametrize("groups", [1, 0, 4, 9])
 @pytest.mark.parametrize("name,kernel", [("full_s", "auto"), ("iq_s", "auto"), ("large_s", "auto"),
-                                         ("full_s", "window"), ("large_s", "window")])
+                                         ("full_s", "window"), ("large_s", "window"),
+                                         ("full_s", "pair"), ("large_s", "pair")])
 def test_host_entry_point_matches_device(oracle, small_problems, name, kernel, groups):
     """Host buffers in, host buffer out: copying everything first (groups=1)
     reproduces the device entry point bit for bit; streaming the record in
@@ -406,7 +402,7 @@ def test_full_size_sampled(oracle, name, samples):
     inputs = device_inputs(prob)
     idx = synth.sample_voxels(prob.N, samples, seed=prob.wl.seed)
     ref, slack = oracle_beamform(oracle, prob, idx=idx)
-    kernels = ["auto", "bi"] + (["window"] if name != "iq" else []) + \
+    kernels = ["auto", "bi", "brick"] + (["window", "pair"] if name != "iq" else []) + \
         (["bl"] if name in ("mid", "full") else [])
     for kernel in kernels:
         y, used = gpu_beamform(prob, kernel, inputs=inputs)

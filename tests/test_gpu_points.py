@@ -13,7 +13,7 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():  # pragma: no cover - CPU containers skip these
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
-KERNELS = ["bl", "bi", "brick", "window"]
+KERNELS = ["bl", "bi", "brick", "window", "pair"]
 
 
 def run_points(prob, pts, tau, w, kernel):
@@ -40,8 +40,8 @@ def oracle_points(oracle, prob, pts, tau, w):
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("base", ["full", "iq"])
 def test_sampled_grid_voxels_as_a_list(oracle, base, kernel):
-    if kernel == "window" and base == "iq":
-        pytest.skip("the window kernel serves float32 records only")
+    if kernel in ("window", "pair") and base == "iq":
+        pytest.skip("the window and pair kernels serve float32 records only")
     prob = synth.make_problem(base, n_el=8, nx=19, ny=13, nz=5)
     rng = np.random.default_rng(21)
     idx = rng.choice(prob.N, 333, replace=False)            # shuffled: no spatial order

@@ -15,7 +15,7 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU containers skip thes
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
 CASES = 24
-KERNELS = ["auto", "bl", "bi", "brick", "window"]
+KERNELS = ["auto", "bl", "bi", "brick", "window", "pair"]
 
 
 def _case(seed):
@@ -38,7 +38,7 @@ def test_kernels_match_oracle_on_random_problem(oracle, seed):
         try:
             y = plan.beamform(*inputs)
         except das.DasError as exc:
-            assert exc.status == das.DAS_ERR_UNSUPPORTED and kernel in ("bi", "brick", "window"), \
+            assert exc.status == das.DAS_ERR_UNSUPPORTED and kernel in ("bi", "brick", "window", "pair"), \
                 (seed, kernel, exc)
             plan.close()
             continue

@@ -63,6 +63,7 @@ struct das_plan_s {
     int *d_order = nullptr;                   // list plans: caller's index of each slot
     Pos64 *d_rx64 = nullptr, *d_vox64 = nullptr;   // double copies, float64 / complex128 plans
     void *d_perm = nullptr;
+    unsigned *d_flag = nullptr;               // set by the permute when the record holds NaN / inf
     size_t perm_bytes = 0;
     bool perm_pads_zero = false;   // scratch holds the padded layout with zero pad rows
     // device staging of das_beamform_host, and its copy stream / events
@@ -149,24 +150,35 @@ std::vector<int> compact_order(const float *xyz, int N)
 das_status check_supported(const das_plan_s *p, int kernel)
 {
     const bool cplx = p->dtype == DAS_C64;
-    if (p->storage == DAS_STORAGE_F16 && kernel != DAS_KERNEL_BRICK)
-        return fail(DAS_ERR_UNSUPPORTED, "half-precision storage is served by the brick kernel only");
+    const bool half = p->storage == DAS_STORAGE_F16;
+    if (half && kernel != DAS_KERNEL_BRICK && kernel != DAS_KERNEL_BI)
+        return fail(DAS_ERR_UNSUPPORTED, "half-precision storage is served by the brick and BI kernels only");
     if (p->is_double() && kernel != DAS_KERNEL_BL)
         return fail(DAS_ERR_UNSUPPORTED, "float64 / complex128 plans are served by the BL kernel only");
     switch (kernel) {
     case DAS_KERNEL_BL: return DAS_OK;
     case DAS_KERNEL_BI:
-        if (p->K < 2 || !das::bi_supported(p->B, cplx, p->bi_group, p->Q, p->M, p->K))
+        if (p->K < 2 || !das::bi_supported(p->B, cplx, p->bi_group, p->Q, p->M, p->K, half))
             return fail(DAS_ERR_UNSUPPORTED,
-                        "BI kernel needs K >= 2, B a multiple of the group's 16-byte chunks, "
-                        "its transmit table in shared memory and a record of < 2^32 16-byte "
-                        "chunks (B=%d, group=%d, Q=%d)", p->B, p->bi_group, p->Q);
+                        "BI kernel needs K >= 2, B a multiple of the group's 16-byte chunks "
+                        "(half storage: one chunk per lane), its transmit table in shared memory "
+                        "and a record of < 2^32 16-byte chunks (B=%d, group=%d, Q=%d)",
+                        p->B, p->bi_group, p->Q);
         return DAS_OK;
     case DAS_KERNEL_BRICK:
-        if (!das::brick_supported(p->B, cplx, p->K, p->storage == DAS_STORAGE_F16))
+        if (!das::brick_supported(p->B, cplx, p->K, half))
             return fail(DAS_ERR_UNSUPPORTED,
                         "brick kernel needs K >= 2 and B * element size in {32, 64, 128, 256, 512} "
                         "bytes (half storage: {16, ..., 64, 128, 256}) (B=%d)", p->B);
+        return DAS_OK;
+    case DAS_KERNEL_PAIR:
+        if (!das::pair_supported(p->B, cplx, p->K))
+            return fail(DAS_ERR_UNSUPPORTED,
+                        "pair kernel needs a float32 record with B in {16, 32, 64} and K >= 2 (B=%d)",
+                        p->B);
+        if (das::pair_smem_bytes(p->B, p->Q) > 227 * 1024)
+            return fail(DAS_ERR_UNSUPPORTED, "pair kernel: transmit table of Q=%d does not fit shared memory",
+                        p->Q);
         return DAS_OK;
     case DAS_KERNEL_WINDOW:
         if (!das::window_supported(p->B, cplx, p->K, p->Q, p->M))
@@ -215,7 +227,7 @@ void release(das_plan_s *p)
     if (p->own) {
         if (p->used && p->done) cudaStreamWaitEvent(p->own, p->done, 0);
         void *bufs[] = {p->d_rx, p->d_vox, p->d_order, p->d_rx64, p->d_vox64,
-                        p->d_perm, p->d_rf, p->d_out, p->d_tau, p->d_w};
+                        p->d_perm, p->d_flag, p->d_rf, p->d_out, p->d_tau, p->d_w};
         for (void *b : bufs)
             if (b) cudaFreeAsync(b, p->own);
     }
@@ -246,6 +258,10 @@ struct DoneMark {
 // the scratch held something else; the permute never writes the pad rows.
 das_status ensure_scratch(das_plan_s *p, int layout, cudaStream_t stream)
 {
+    if (!p->d_flag) {
+        cudaError_t e = plan_alloc(p, &p->d_flag, 256);
+        if (e != cudaSuccess) return cuda_fail(e, "flag allocation");
+    }
     if (!p->d_perm) {
         cudaError_t e = plan_alloc(p, &p->d_perm, p->padded_bytes());
         if (e != cudaSuccess) return cuda_fail(e, "permute scratch allocation");
@@ -456,7 +472,7 @@ das_status das_plan_set_option(das_plan p, int option, double value)
     switch (option) {
     case DAS_OPT_KERNEL: {
         const int k = (int)value;
-        if ((double)k != value || k < DAS_KERNEL_AUTO || k > DAS_KERNEL_WINDOW)
+        if ((double)k != value || k < DAS_KERNEL_AUTO || k > DAS_KERNEL_PAIR)
             return fail(DAS_ERR_INVALID_ARG, "invalid kernel %g", value);
         p->kernel = k;
         return DAS_OK;
@@ -555,9 +571,12 @@ das_status das_beamform(das_plan p, const void *rf, const float *tau_tx, const f
     cudaError_t e = cudaSuccess;
     if (p->timing) e = cudaEventRecord(p->ev[0], stream);
     const bool half = p->storage == DAS_STORAGE_F16;
+    // the pair kernel needs to know whether the record holds a non-finite sample
+    unsigned *flag = kernel == DAS_KERNEL_PAIR ? p->d_flag : nullptr;
+    if (e == cudaSuccess && flag) e = cudaMemsetAsync(flag, 0, sizeof(unsigned), stream);
     if (e == cudaSuccess && permute) {
         e = das::launch_permute(rf, p->d_perm, (int)p->elem_bytes(), p->B, p->Q, p->M, p->K,
-                                layout, p->num_sms, stream, 0, -1, half);
+                                layout, p->num_sms, stream, 0, -1, half, flag);
         src = p->d_perm;
     }
     if (e == cudaSuccess && p->timing) e = cudaEventRecord(p->ev[1], stream);
@@ -568,10 +587,13 @@ das_status das_beamform(das_plan p, const void *rf, const float *tau_tx, const f
                            : das::launch_bl(p->geom, p->d_rx, src, tau_tx, w_tx, out, cplx, stream);
         break;
     case DAS_KERNEL_BI:
-        e = das::launch_bi(p->geom, p->d_rx, src, tau_tx, w_tx, out, cplx, p->bi_group, stream);
+        e = das::launch_bi(p->geom, p->d_rx, src, tau_tx, w_tx, out, cplx, p->bi_group, stream, half);
         break;
     case DAS_KERNEL_WINDOW:
         e = das::launch_window(p->geom, p->d_rx, src, tau_tx, w_tx, out, stream);
+        break;
+    case DAS_KERNEL_PAIR:
+        e = das::launch_pair(p->geom, p->d_rx, src, tau_tx, w_tx, out, flag, stream);
         break;
     default:
         e = das::launch_brick(p->geom, p->d_rx, src, tau_tx, w_tx, out, cplx, stream, 0, -1, false, half);
@@ -604,7 +626,7 @@ das_status das_beamform_host(das_plan p, const void *rf_host, const float *tau_t
     if (e != cudaSuccess) return cuda_fail(e, "host-path device buffers");
     DoneMark mark{p, stream};
     int groups = p->host_groups > 0 ? p->host_groups : (p->Q < 5 ? p->Q : 5);
-    if (kernel != DAS_KERNEL_BRICK && kernel != DAS_KERNEL_WINDOW)
+    if (kernel != DAS_KERNEL_BRICK && kernel != DAS_KERNEL_WINDOW && kernel != DAS_KERNEL_PAIR)
         groups = 1;                                  // only these kernels sum transmit ranges
     if (groups > p->Q) groups = p->Q;
 
@@ -648,18 +670,23 @@ das_status das_beamform_host(das_plan p, const void *rf_host, const float *tau_t
         if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
         st = ensure_scratch(p, 2, stream);
         if (st != DAS_OK) return st;
+        unsigned *flag = kernel == DAS_KERNEL_PAIR ? p->d_flag : nullptr;
         e = cudaStreamWaitEvent(stream, p->copy_ev[1], 0);
+        if (e == cudaSuccess && flag) e = cudaMemsetAsync(flag, 0, sizeof(unsigned), stream);
         for (int gi = 0; gi < groups && e == cudaSuccess; ++gi) {
             const int q0 = gi * p->Q / groups, q1 = (gi + 1) * p->Q / groups;
             e = cudaStreamWaitEvent(stream, p->copy_ev[2 + gi], 0);
             const bool half = p->storage == DAS_STORAGE_F16;
             if (e == cudaSuccess)
                 e = das::launch_permute(p->d_rf, p->d_perm, (int)eb, p->B, p->Q, p->M, p->K, 2,
-                                        p->num_sms, stream, q0, q1, half);
+                                        p->num_sms, stream, q0, q1, half, flag);
             if (e == cudaSuccess)
                 e = kernel == DAS_KERNEL_WINDOW
                         ? das::launch_window(p->geom, p->d_rx, p->d_perm, p->d_tau, p->d_w, p->d_out,
                                              stream, q0, q1, gi > 0)
+                    : kernel == DAS_KERNEL_PAIR
+                        ? das::launch_pair(p->geom, p->d_rx, p->d_perm, p->d_tau, p->d_w, p->d_out,
+                                           flag, stream, q0, q1, gi > 0)
                         : das::launch_brick(p->geom, p->d_rx, p->d_perm, p->d_tau, p->d_w, p->d_out,
                                             cplx, stream, q0, q1, gi > 0, half);
         }
@@ -688,6 +715,7 @@ das_status das_plan_device_bytes(das_plan p, size_t *bytes)
 {
     if (!p || !bytes) return fail(DAS_ERR_INVALID_ARG, "NULL argument");
     size_t b = sizeof(RxPos) * p->M + p->perm_bytes + (p->d_vox ? sizeof(float4) * (size_t)p->N : 0);
+    if (p->d_flag) b += 256;
     if (p->d_order) b += sizeof(int) * (size_t)p->N;
     if (p->d_rx64) b += sizeof(Pos64) * p->M;
     if (p->d_vox64) b += sizeof(Pos64) * (size_t)p->N;

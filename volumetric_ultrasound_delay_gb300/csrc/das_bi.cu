@@ -16,6 +16,14 @@
 // row and its two weights, and issuing the row loads of the U receivers
 // before their FMAs.  Real frames are accumulated in pairs
 // with the packed FP32 FMA (__ffma2_rn).
+//
+// With half-precision storage (the pages' BI-FP16 variant: ffdas paper,
+// Methods, FP16 paragraphs; ffdas docs, "Mixed-precision storage") the copy
+// holds half (real) or half2 (IQ) samples, a 16-byte chunk carries twice as
+// many frames, and each is converted to float32 before the interpolation and
+// the accumulation.
+#include <cuda_fp16.h>
+
 #include "das_device.cuh"
 
 #ifndef DAS_BI_U
@@ -38,13 +46,34 @@ constexpr int MIN_BLOCKS = 24;
 template <bool CPLX>
 constexpr int walk_step() { return CPLX ? 1 : DAS_BI_U; }
 
-template <int G, int J, bool CPLX>
+// elements per 16-byte chunk of the copy
+template <bool CPLX, bool HALF>
+constexpr int chunk_elems() { return HALF ? (CPLX ? 4 : 8) : (CPLX ? 2 : 4); }
+
+// 16 bytes of samples -> NPC float2 values in float32: frame pairs (real) or
+// one complex frame each (IQ)
+template <bool HALF, int NPC>
+__device__ __forceinline__ void unpack_chunk(uint4 u, float2 (&v)[NPC])
+{
+    if constexpr (HALF) {
+        const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+        for (int i = 0; i < NPC; ++i) v[i] = __half22float2(h[i]);
+    } else {
+        const float2 *f = reinterpret_cast<const float2 *>(&u);
+#pragma unroll
+        for (int i = 0; i < NPC; ++i) v[i] = f[i];
+    }
+}
+
+template <int G, int J, bool CPLX, bool HALF>
 __global__ void __launch_bounds__(THREADS, MIN_BLOCKS)
-das_bi_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__ perm,
+das_bi_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict__ perm,
               const float *__restrict__ tau, const float *__restrict__ wtx, float *__restrict__ out)
 {
     constexpr int NW = 32 / G;                    // voxels per warp
-    constexpr int CH = CPLX ? 2 : 4;              // elements per 16-byte chunk
+    constexpr int CH = chunk_elems<CPLX, HALF>(); // elements per 16-byte chunk
+    constexpr int NPC = CPLX ? CH : CH / 2;       // float2 accumulators per chunk
     constexpr int U = walk_step<CPLX>();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -56,7 +85,7 @@ das_bi_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__
     const float3 p = nvalid ? voxel_position(g, s) : make_float3(0.f, 0.f, 0.f);
     const int n = nvalid ? voxel_index(g, s) : 0;
     const long long qmb = (long long)g.Q * g.M * g.B;        // row stride of k
-    const float4 *perm4 = reinterpret_cast<const float4 *>(perm) + t;   // chunk t of a row
+    const uint4 *perm4 = reinterpret_cast<const uint4 *>(perm) + t;     // chunk t of a row
     const long long qmbc = qmb / CH;                                    // row stride in chunks
     const long long bc = g.B / CH;                                      // chunks per (q, m) row
 
@@ -76,10 +105,12 @@ das_bi_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__
     __syncthreads();
     const float2 *txv = txs + (warp * NW + grp) * g.Q;
 
-    // real: frame pairs (2 per chunk); IQ: one complex frame each (2 per chunk)
-    float2 acc[J][2];
+    // real: frame pairs; IQ: one complex frame each (NPC per chunk)
+    float2 acc[J][NPC];
 #pragma unroll
-    for (int c = 0; c < J; ++c) acc[c][0] = acc[c][1] = make_float2(0.f, 0.f);
+    for (int c = 0; c < J; ++c)
+#pragma unroll
+        for (int i = 0; i < NPC; ++i) acc[c][i] = make_float2(0.f, 0.f);
 
     for (int m0 = 0; m0 < g.M; m0 += G) {
         // ---- this lane's receiver m0 + t: distance and aperture, for every q
@@ -116,7 +147,7 @@ das_bi_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__
                     src[u] = use[u] ? __ffs(mine) - 1 : src[0];
                     mine &= mine - 1u;
                 }
-                float4 v0[U][J], v1[U][J];
+                uint4 v0[U][J], v1[U][J];
                 float2 W0[U], W1[U];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
@@ -130,12 +161,12 @@ das_bi_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__
                     }
                     W0[u] = CPLX ? make_float2(a0 * pj.x, a0 * pj.y) : make_float2(a0, a0);
                     W1[u] = CPLX ? make_float2(a1 * pj.x, a1 * pj.y) : make_float2(a1, a1);
-                    const float4 *p0 = perm4 + cj;
+                    const uint4 *p0 = perm4 + cj;
                     // a row standing in for a sample outside the record is not read
                     const bool r0_in = use[u] && !skip_row(a0), r1_in = use[u] && !skip_row(a1);
 #pragma unroll
                     for (int c = 0; c < J; ++c) {
-                        v0[u][c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        v0[u][c] = make_uint4(0u, 0u, 0u, 0u);
                         v1[u][c] = v0[u][c];
                         if (r0_in) v0[u][c] = __ldg(p0 + c * G);
                         if (r1_in) v1[u][c] = __ldg(p0 + qmbc + c * G);
@@ -146,18 +177,18 @@ das_bi_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__
                     if (!use[u]) break;
 #pragma unroll
                     for (int c = 0; c < J; ++c) {
-                        const float2 x0 = make_float2(v0[u][c].x, v0[u][c].y), y0 = make_float2(v0[u][c].z, v0[u][c].w);
-                        const float2 x1 = make_float2(v1[u][c].x, v1[u][c].y), y1 = make_float2(v1[u][c].z, v1[u][c].w);
-                        if constexpr (CPLX) {
-                            cfma(acc[c][0], W1[u], x1);
-                            cfma(acc[c][1], W1[u], y1);
-                            cfma(acc[c][0], W0[u], x0);
-                            cfma(acc[c][1], W0[u], y0);
-                        } else {
-                            acc[c][0] = __ffma2_rn(W1[u], x1, acc[c][0]);
-                            acc[c][1] = __ffma2_rn(W1[u], y1, acc[c][1]);
-                            acc[c][0] = __ffma2_rn(W0[u], x0, acc[c][0]);
-                            acc[c][1] = __ffma2_rn(W0[u], y0, acc[c][1]);
+                        float2 x0[NPC], x1[NPC];
+                        unpack_chunk<HALF, NPC>(v0[u][c], x0);
+                        unpack_chunk<HALF, NPC>(v1[u][c], x1);
+#pragma unroll
+                        for (int i = 0; i < NPC; ++i) {
+                            if constexpr (CPLX) {
+                                cfma(acc[c][i], W1[u], x1[i]);
+                                cfma(acc[c][i], W0[u], x0[i]);
+                            } else {
+                                acc[c][i] = __ffma2_rn(W1[u], x1[i], acc[c][i]);
+                                acc[c][i] = __ffma2_rn(W0[u], x0[i], acc[c][i]);
+                            }
                         }
                     }
                 }
@@ -168,15 +199,14 @@ das_bi_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__
 #pragma unroll
     for (int c = 0; c < J; ++c) {
         const long long e0 = (long long)(t + c * G) * CH;     // first element of the lane's chunk
-        if constexpr (CPLX) {
-            float2 *o = reinterpret_cast<float2 *>(out);
-            o[(e0 + 0) * g.N + n] = acc[c][0];
-            o[(e0 + 1) * g.N + n] = acc[c][1];
-        } else {
-            out[(e0 + 0) * g.N + n] = acc[c][0].x;
-            out[(e0 + 1) * g.N + n] = acc[c][0].y;
-            out[(e0 + 2) * g.N + n] = acc[c][1].x;
-            out[(e0 + 3) * g.N + n] = acc[c][1].y;
+#pragma unroll
+        for (int i = 0; i < NPC; ++i) {
+            if constexpr (CPLX) {
+                reinterpret_cast<float2 *>(out)[(e0 + i) * g.N + n] = acc[c][i];
+            } else {
+                out[(e0 + 2 * i) * g.N + n] = acc[c][i].x;
+                out[(e0 + 2 * i + 1) * g.N + n] = acc[c][i].y;
+            }
         }
     }
 }
@@ -185,7 +215,7 @@ das_bi_kernel(DasGeom g, const RxPos *__restrict__ rx, const float *__restrict__
 size_t smem_bytes(int G, int Q) { return sizeof(float2) * (size_t)(THREADS / 32) * (32 / G) * Q; }
 constexpr size_t SMEM_MAX = 227 * 1024;
 
-template <int G, int J, bool CPLX>
+template <int G, int J, bool CPLX, bool HALF>
 cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
                        const float *w, void *out, cudaStream_t stream)
 {
@@ -195,52 +225,58 @@ cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, cons
     const size_t smem = smem_bytes(G, g.Q);
     if (smem > SMEM_MAX) return cudaErrorInvalidValue;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(das_bi_kernel<G, J, CPLX>,
+        cudaError_t e = cudaFuncSetAttribute(das_bi_kernel<G, J, CPLX, HALF>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    das_bi_kernel<G, J, CPLX><<<grid, THREADS, smem, stream>>>(
-        g, rx, static_cast<const float *>(perm), tau, w, static_cast<float *>(out));
+    das_bi_kernel<G, J, CPLX, HALF><<<grid, THREADS, smem, stream>>>(
+        g, rx, perm, tau, w, static_cast<float *>(out));
     return cudaGetLastError();
 }
 
 // lanes per voxel G (default: 16-byte chunks per voxel capped at 16, as the
-// pages' N_warp = 2 design) and chunks per lane J
-bool choose(int B, bool cplx, int group, int &G, int &J)
+// pages' N_warp = 2 design) and chunks per lane J; half storage takes one
+// chunk per lane (J = 1)
+bool choose(int B, bool cplx, bool half, int group, int &G, int &J)
 {
-    const int ch = cplx ? 2 : 4;
+    const int ch = half ? (cplx ? 4 : 8) : (cplx ? 2 : 4);
     if (B % ch != 0) return false;
     const int chunks = B / ch;
     G = group > 0 ? group : (chunks < 16 ? chunks : 16);
     if (G != 2 && G != 4 && G != 8 && G != 16 && G != 32) return false;
     if (chunks % G != 0) return false;
     J = chunks / G;
-    return J == 1 || J == 2 || J == 4;
+    return half ? J == 1 : (J == 1 || J == 2 || J == 4);
 }
 
 }  // namespace
 
-bool bi_supported(int B, bool cplx, int group, int Q, int M, int K)
+bool bi_supported(int B, bool cplx, int group, int Q, int M, int K, bool half)
 {
     int G, J;
     // row indices travel as 32-bit counts of 16-byte chunks
-    const long long chunks = (long long)K * Q * M * B / (cplx ? 2 : 4);
-    return choose(B, cplx, group, G, J) && smem_bytes(G, Q) <= SMEM_MAX && chunks < (1LL << 32);
+    const long long chunks = (long long)K * Q * M * B / (half ? (cplx ? 4 : 8) : (cplx ? 2 : 4));
+    return choose(B, cplx, half, group, G, J) && smem_bytes(G, Q) <= SMEM_MAX && chunks < (1LL << 32);
 }
 
 cudaError_t launch_bi(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
-                      const float *w, void *out, bool cplx, int group, cudaStream_t stream)
+                      const float *w, void *out, bool cplx, int group, cudaStream_t stream, bool half)
 {
     int G, J;
-    if (!bi_supported(g.B, cplx, group, g.Q, g.M, g.K) || !choose(g.B, cplx, group, G, J))
+    if (!bi_supported(g.B, cplx, group, g.Q, g.M, g.K, half) || !choose(g.B, cplx, half, group, G, J))
         return cudaErrorInvalidValue;
-#define DAS_BI_CASE(GG, JJ)                                                                     \
-    if (G == GG && J == JJ)                                                                     \
-        return cplx ? launch_one<GG, JJ, true>(g, rx, perm, tau, w, out, stream)                \
-                    : launch_one<GG, JJ, false>(g, rx, perm, tau, w, out, stream);
-    DAS_BI_CASE(2, 1) DAS_BI_CASE(4, 1) DAS_BI_CASE(8, 1) DAS_BI_CASE(16, 1) DAS_BI_CASE(32, 1)
-    DAS_BI_CASE(2, 2) DAS_BI_CASE(4, 2) DAS_BI_CASE(8, 2) DAS_BI_CASE(16, 2) DAS_BI_CASE(32, 2)
-    DAS_BI_CASE(2, 4) DAS_BI_CASE(4, 4) DAS_BI_CASE(8, 4) DAS_BI_CASE(16, 4) DAS_BI_CASE(32, 4)
+#define DAS_BI_CASE(GG, JJ, HH)                                                                 \
+    if (G == GG && J == JJ && half == HH)                                                       \
+        return cplx ? launch_one<GG, JJ, true, HH>(g, rx, perm, tau, w, out, stream)            \
+                    : launch_one<GG, JJ, false, HH>(g, rx, perm, tau, w, out, stream);
+    DAS_BI_CASE(2, 1, false) DAS_BI_CASE(4, 1, false) DAS_BI_CASE(8, 1, false)
+    DAS_BI_CASE(16, 1, false) DAS_BI_CASE(32, 1, false)
+    DAS_BI_CASE(2, 2, false) DAS_BI_CASE(4, 2, false) DAS_BI_CASE(8, 2, false)
+    DAS_BI_CASE(16, 2, false) DAS_BI_CASE(32, 2, false)
+    DAS_BI_CASE(2, 4, false) DAS_BI_CASE(4, 4, false) DAS_BI_CASE(8, 4, false)
+    DAS_BI_CASE(16, 4, false) DAS_BI_CASE(32, 4, false)
+    DAS_BI_CASE(2, 1, true) DAS_BI_CASE(4, 1, true) DAS_BI_CASE(8, 1, true)
+    DAS_BI_CASE(16, 1, true) DAS_BI_CASE(32, 1, true)
 #undef DAS_BI_CASE
     return cudaErrorInvalidValue;
 }

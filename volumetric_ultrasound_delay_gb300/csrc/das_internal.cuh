@@ -51,23 +51,34 @@ void record_error(const char *msg);
 
 // Launchers (each returns the cudaError_t of its launch).
 // Permutes the planes of transmits [q0, q1) (q1 < 0: all Q); to_half converts
-// float32 / complex64 elements to half / half2 on the way.
+// float32 / complex64 elements to half / half2 on the way; nonfinite (device,
+// optional) is set to 1 when a permuted float32 value is NaN or inf.
 cudaError_t launch_permute(const void *in, void *out, int elem_bytes, int B, int Q, int M, int K,
                            int layout, int num_sms, cudaStream_t stream, int q0 = 0, int q1 = -1,
-                           bool to_half = false);
+                           bool to_half = false, unsigned *nonfinite = nullptr);
 cudaError_t launch_bl(const DasGeom &g, const RxPos *rx, const void *rf, const float *tau,
                       const float *w, void *out, bool cplx, cudaStream_t stream);
 cudaError_t launch_bl64(const DasGeom64 &g, const Pos64 *rx, const void *rf, const float *tau,
                         const float *w, void *out, bool cplx, cudaStream_t stream);
-bool bi_supported(int B, bool cplx, int group, int Q, int M, int K);
+// half: perm holds half / half2 samples (K x Q x M x B)
+bool bi_supported(int B, bool cplx, int group, int Q, int M, int K, bool half = false);
 cudaError_t launch_bi(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
-                      const float *w, void *out, bool cplx, int group, cudaStream_t stream);
+                      const float *w, void *out, bool cplx, int group, cudaStream_t stream,
+                      bool half = false);
 bool brick_supported(int B, bool cplx, int K, bool half = false);
 // Sums transmits [q0, q1) (q1 < 0: all Q); with accumulate, adds to out
 // instead of overwriting it; half: perm holds half / half2 samples.
 cudaError_t launch_brick(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
                          const float *w, void *out, bool cplx, cudaStream_t stream, int q0 = 0,
                          int q1 = -1, bool accumulate = false, bool half = false);
+bool pair_supported(int B, bool cplx, int K, bool half = false);
+size_t pair_smem_bytes(int B, int Q);
+// float32 records; nonfinite: the flag the permute of this record set (the
+// kernel then adds each term to its own voxel only); transmits [q0, q1),
+// accumulate as for the brick kernel
+cudaError_t launch_pair(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
+                        const float *w, void *out, const unsigned *nonfinite, cudaStream_t stream,
+                        int q0 = 0, int q1 = -1, bool accumulate = false);
 bool window_supported(int B, bool cplx, int K, int Q, int M, bool half = false);
 // float32 records only; transmits [q0, q1), accumulate as for the brick kernel
 cudaError_t launch_window(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,

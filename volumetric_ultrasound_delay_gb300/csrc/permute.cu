@@ -18,6 +18,11 @@
 // With half-precision storage the copy converts float32 -> half and complex64
 // -> half2 (round to nearest) as it writes: the pages' FP16 variants fuse that
 // conversion into the permute (ffdas paper, Methods, FP16 paragraphs).
+//
+// On request the copy also reports whether the record holds a non-finite
+// float32 value (NaN or inf, any component): it sets *nonfinite to 1, which
+// the caller clears beforehand.  The pair kernel reads that flag to decide
+// whether zero weights may multiply samples (see das_pair.cu).
 #include <cuda_fp16.h>
 
 #include <cstdint>
@@ -41,6 +46,9 @@ constexpr int sub_tiles() { return sizeof(T) >= 8 ? 2 : 4; }
 // (round to nearest) for half-precision storage of the copy
 template <typename TO, typename TI>
 __device__ __forceinline__ TO convert(TI v) { return v; }
+
+// 1 if a 32-bit word is a float32 NaN or inf
+__device__ __forceinline__ unsigned not_finite(unsigned w) { return (w & 0x7f800000u) == 0x7f800000u; }
 template <>
 __device__ __forceinline__ __half convert<__half, float>(float v) { return __float2half_rn(v); }
 template <>
@@ -50,8 +58,11 @@ template <typename T, typename TO>
 __global__ void __launch_bounds__(THREADS)
 permute_kernel(const T *__restrict__ in, TO *__restrict__ out, int B, int QM, int K,
                long long osk, long long osqm, long long n_blocks, int blocks_b, int blocks_k,
-               int vec_in, int vec_out, int qm0)
+               int vec_in, int vec_out, int qm0, unsigned *__restrict__ nonfinite)
 {
+    // float data (4- and 8-byte elements) can be checked for non-finite values
+    constexpr bool FLOATS = sizeof(T) % 4 == 0;
+    unsigned bad = 0u;
     constexpr int V = 16 / sizeof(T);            // input elements per 16-byte vector
     constexpr int VPR = TILE / V;                // input vectors per 32-element row
     constexpr int VO = 16 / sizeof(TO);          // output elements per 16-byte vector
@@ -78,6 +89,8 @@ permute_kernel(const T *__restrict__ in, TO *__restrict__ out, int B, int QM, in
                     if (b < B && k < K) {   // K % V == 0, so the whole vector is inside
                         const uint4 u = __ldg(reinterpret_cast<const uint4 *>(
                             in + ((long long)b * QM + qm) * K + k));
+                        if (FLOATS && nonfinite)
+                            bad |= not_finite(u.x) | not_finite(u.y) | not_finite(u.z) | not_finite(u.w);
                         T vals[V];
                         memcpy(vals, &u, sizeof(u));
 #pragma unroll
@@ -90,7 +103,18 @@ permute_kernel(const T *__restrict__ in, TO *__restrict__ out, int B, int QM, in
                 for (int i = tid; i < TILE * TILE; i += THREADS) {
                     const int row = i / TILE, kk = i % TILE;
                     const int b = b0 + row, k = k0 + s * TILE + kk;
-                    if (b < B && k < K) tile[s][row][kk] = in[((long long)b * QM + qm) * K + k];
+                    if (b < B && k < K) {
+                        const T v = in[((long long)b * QM + qm) * K + k];
+                        if constexpr (FLOATS) {
+                            if (nonfinite) {
+                                unsigned w[sizeof(T) / 4];
+                                memcpy(w, &v, sizeof(T));
+#pragma unroll
+                                for (int j = 0; j < (int)(sizeof(T) / 4); ++j) bad |= not_finite(w[j]);
+                            }
+                        }
+                        tile[s][row][kk] = v;
+                    }
                 }
         }
         __syncthreads();
@@ -123,11 +147,15 @@ permute_kernel(const T *__restrict__ in, TO *__restrict__ out, int B, int QM, in
         }
         __syncthreads();
     }
+    if (nonfinite) {
+        const unsigned any = __ballot_sync(0xffffffffu, bad != 0u);
+        if (any != 0u && (threadIdx.x & 31) == __ffs(any) - 1) atomicOr(nonfinite, 1u);
+    }
 }
 
 template <typename T, typename TO = T>
 cudaError_t launch_typed(const void *in, void *out, int B, int Q, int M, int K, int layout,
-                         int num_sms, cudaStream_t stream, int q0, int q1)
+                         int num_sms, cudaStream_t stream, int q0, int q1, unsigned *nonfinite)
 {
     constexpr int V = 16 / sizeof(T);
     constexpr int VO = 16 / sizeof(TO);
@@ -149,7 +177,7 @@ cudaError_t launch_typed(const void *in, void *out, int B, int Q, int M, int K, 
     const int grid = (int)(n_blocks < cap ? n_blocks : cap);
     permute_kernel<T, TO><<<grid, THREADS, 0, stream>>>(
         static_cast<const T *>(in), static_cast<TO *>(out), B, QM, K, osk, osqm, n_blocks,
-        blocks_b, blocks_k, vec_in, vec_out, q0 * M);
+        blocks_b, blocks_k, vec_in, vec_out, q0 * M, nonfinite);
     return cudaGetLastError();
 }
 
@@ -157,21 +185,21 @@ cudaError_t launch_typed(const void *in, void *out, int B, int Q, int M, int K, 
 
 cudaError_t launch_permute(const void *in, void *out, int elem_bytes, int B, int Q, int M, int K,
                            int layout, int num_sms, cudaStream_t stream, int q0, int q1,
-                           bool to_half)
+                           bool to_half, unsigned *nonfinite)
 {
     if (q1 < 0) q1 = Q;
     if (q0 < 0 || q0 > q1 || q1 > Q) return cudaErrorInvalidValue;
     if (to_half) {
         switch (elem_bytes) {
-        case 4: return launch_typed<float, __half>(in, out, B, Q, M, K, layout, num_sms, stream, q0, q1);
-        case 8: return launch_typed<float2, __half2>(in, out, B, Q, M, K, layout, num_sms, stream, q0, q1);
+        case 4: return launch_typed<float, __half>(in, out, B, Q, M, K, layout, num_sms, stream, q0, q1, nonfinite);
+        case 8: return launch_typed<float2, __half2>(in, out, B, Q, M, K, layout, num_sms, stream, q0, q1, nonfinite);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (elem_bytes) {
-    case 2: return launch_typed<unsigned short>(in, out, B, Q, M, K, layout, num_sms, stream, q0, q1);
-    case 4: return launch_typed<float>(in, out, B, Q, M, K, layout, num_sms, stream, q0, q1);
-    case 8: return launch_typed<float2>(in, out, B, Q, M, K, layout, num_sms, stream, q0, q1);
+    case 2: return launch_typed<unsigned short>(in, out, B, Q, M, K, layout, num_sms, stream, q0, q1, nonfinite);
+    case 4: return launch_typed<float>(in, out, B, Q, M, K, layout, num_sms, stream, q0, q1, nonfinite);
+    case 8: return launch_typed<float2>(in, out, B, Q, M, K, layout, num_sms, stream, q0, q1, nonfinite);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -22,7 +22,7 @@ DAS_OK, DAS_ERR_INVALID_ARG, DAS_ERR_UNSUPPORTED, DAS_ERR_OUT_OF_MEMORY, DAS_ERR
     DAS_ERR_TIMEOUT = range(6)
 DAS_F32, DAS_C64, DAS_F64, DAS_C128 = 0, 1, 2, 3
 _DTYPES = {"f32": DAS_F32, "c64": DAS_C64, "f64": DAS_F64, "c128": DAS_C128}
-KERNELS = {"auto": 0, "bl": 1, "bi": 2, "brick": 3, "window": 4}
+KERNELS = {"auto": 0, "bl": 1, "bi": 2, "brick": 3, "window": 4, "pair": 5}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 OPT_KERNEL, OPT_DEMOD_HZ, OPT_TIMING, OPT_BI_GROUP, OPT_HOST_GROUPS, OPT_STORAGE = 0, 1, 2, 3, 4, 5
 STORAGE_NATIVE, STORAGE_F16 = 0, 1
