@@ -23,7 +23,10 @@ Prints ONE JSON line (rank 0).  Besides the device-timed value it reports:
                 two_threads: a stream of volumes on two plans, one host thread each;
   clocks        SM clocks and throttle reasons sampled during the timed region;
   pipeline      volumes alternating between two plans on two streams (the
-                permute of one overlaps the DAS kernel of the other), per volume.
+                permute of one overlaps the DAS kernel of the other), per volume;
+  relative      every kernel (and half-precision storage where a kernel takes
+                it) on the same workload, DAS-kernel time by CUDA events, with
+                the two ratios the pages report: BI over BL and BI-FP16 over BI.
 
 ``--impl reference`` times the oracle itself (the reference arm: a plain CPU
 program) on bounded samples of the same workload.  Under torchrun with N > 1
@@ -80,6 +83,8 @@ def parse_args():
                     help="override: voxel grid (for small profiling cases)")
     ap.add_argument("--storage", default="native", choices=["native", "f16"],
                     help="element type of the permuted record copy (f16: half precision)")
+    ap.add_argument("--relative-steps", type=int, default=3,
+                    help="timed calls per kernel of the relative table (0 = no table)")
     return ap.parse_args()
 
 
@@ -251,6 +256,53 @@ def measured_traffic(kernel: str, workload: str, storage: str = "native"):
     return r.get("dram_bytes_per_launch")
 
 
+def relative_table(args, prob, rf, tau, w, out, stream, dev):
+    """DAS-kernel milliseconds of every kernel that serves the workload, float32
+    and half-precision storage, by the CUDA events the library records on the
+    launching stream (mean of the timed calls after two warm-up calls), and the
+    pages' two relative measurements: batch-inner over the per-voxel baseline,
+    and half-precision storage over float32 on the batch-inner kernel (ffdas
+    paper, Results, Fig. 2A-C; ffdas docs, ALG2 and "Mixed-precision storage")."""
+    import torch
+    from volumetric_ultrasound_delay_gb300 import das
+    dtype = "c64" if prob.wl.iq else "f32"
+    A = prob.B * prob.N * prob.Q * prob.M
+    rows = {}
+    for kernel, storage in [("bl", "native"), ("bi", "native"), ("bi", "f16"), ("brick", "native"),
+                            ("brick", "f16"), ("window", "native"), ("pair", "native")]:
+        try:
+            plan = das.Plan(prob.grid, prob.rx, prob.c, prob.fs, prob.t0, prob.fnum, dtype, prob.B,
+                            prob.Q, prob.M, prob.K, kernel=kernel, f_demod=prob.f_demod,
+                            storage=storage)
+        except das.DasError:
+            continue
+        plan.set_option(das.OPT_TIMING, 1)
+        try:
+            for _ in range(2):
+                plan.beamform(rf, tau, w, out, stream=stream)
+            ms = []
+            for _ in range(args.relative_steps):
+                plan.beamform(rf, tau, w, out, stream=stream)
+                ms.append(plan.last_times()[1])
+        except das.DasError:
+            plan.close()
+            continue
+        torch.cuda.synchronize(dev)
+        plan.close()
+        das_ms = statistics.mean(ms)
+        rows[f"{kernel}/{storage}"] = {"das_ms": das_ms, "value": A / (das_ms / 1e3)}
+    ratios = {}
+    if "bi/native" in rows and "bl/native" in rows:
+        ratios["bi_over_bl"] = rows["bl/native"]["das_ms"] / rows["bi/native"]["das_ms"]
+    if "bi/f16" in rows and "bi/native" in rows:
+        ratios["bi_f16_over_bi"] = rows["bi/native"]["das_ms"] / rows["bi/f16"]["das_ms"]
+    if "brick/f16" in rows and "brick/native" in rows:
+        ratios["brick_f16_over_brick"] = rows["brick/native"]["das_ms"] / rows["brick/f16"]["das_ms"]
+    return {"kernels": rows, "ratios": ratios, "unit": UNIT,
+            "note": "DAS kernel only (permute excluded), mean of timed calls; ratios are speed-ups; "
+                    "the pages quote BI about 1.4x BL and FP16 storage about 1.2x, hardware unstated"}
+
+
 # ------------------------------------------------------------- arms
 def run_reference(args, world, rank):
     if rank != 0:
@@ -420,6 +472,13 @@ def run_ours(args, world, rank, local):
                                           "copies of every volume inside the timed region"}
             plan_b.close()
 
+    # ---------------- every kernel on the same workload (the pages' relative figures)
+    relative = None
+    if args.relative_steps > 0 and rank == 0:
+        plan.set_option(das.OPT_TIMING, 0)
+        relative = relative_table(args, prob, rf, tau, w, out, stream, dev)
+        plan.set_option(das.OPT_TIMING, 1)
+
     # ---------------- two plans on two streams, volumes alternating (optional)
     pipeline = None
     if args.pipeline > 0 and not flush:
@@ -530,6 +589,8 @@ def run_ours(args, world, rank, local):
     }
     if pipeline is not None:
         line["pipeline"] = pipeline
+    if relative is not None:
+        line["relative"] = relative
     print(json.dumps(line), flush=True)
 
 

@@ -108,6 +108,13 @@ typedef enum {
                               das_plan_last_times); 0 (default): no events */
     DAS_OPT_BI_GROUP = 3,  /* BI kernel: lanes per voxel G in {2,4,8,16,32}; 0 = automatic */
     DAS_OPT_STORAGE = 5,   /* das_storage value: element type of the permuted copy */
+    DAS_OPT_RX_GROUPS = 6, /* das_beamform with the brick kernel: number of launches the
+                              receivers are split into (contiguous blocks of 32 receivers;
+                              each launch adds its receivers' terms to y), so the CTAs
+                              resident at one time read a 1/R share of the record; 1
+                              (default) = one launch, 0 = enough launches for one share to
+                              fit in half the L2.  Changes the float32 summation order,
+                              not the result beyond it */
     DAS_OPT_HOST_GROUPS = 4 /* das_beamform_host with the brick or window kernel: number of transmit
                               groups the record is streamed in (copy of group g+1
                               overlapping the permute and sum of group g); 0 (default) =
@@ -264,8 +271,11 @@ das_status das_plan_destroy(das_plan plan);
  *   layout 2: Q x M x (K+3) x B, sample k of slab (q, m) at row k + 1; rows 0,
  *             K + 1 and K + 2 of every slab are not written (the brick kernel
  *             keeps them zero, so reads just outside the record return 0)
+ *   layout 3: (K+2) x Q x M x B, sample k at plane k + 1; planes 0 and K + 1
+ *             are not written (the BI kernel keeps them zero)
  *   in       device buffer of B*Q*M*K elements of dtype;
- *   out      device buffer of B*Q*M*K (layouts 0, 1) or B*Q*M*(K+3) (layout 2)
+ *   out      device buffer of B*Q*M*K (layouts 0, 1), B*Q*M*(K+3) (layout 2) or
+ *            B*Q*M*(K+2) (layout 3)
  *            elements of dtype, or of half / half2 with DAS_STORAGE_F16; in and
  *            out must not overlap, and each must be aligned to its element
  *            size (16-byte alignment, with K and B multiples of a 16-byte

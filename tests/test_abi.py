@@ -68,7 +68,7 @@ def test_host_side_rejections(libdas):
     assert libdas.das_permute(None, None, 0, 1, 1, 1, 1, 0, 0, None) == das.DAS_ERR_INVALID_ARG
     buf = ctypes.create_string_buffer(64)
     assert libdas.das_permute(buf, buf, 0, 1, 1, 1, 4, 0, 0, None) == das.DAS_ERR_INVALID_ARG  # overlap
-    assert libdas.das_permute(buf, ctypes.byref(buf, 32), 0, 1, 1, 1, 4, 3, 0, None) == das.DAS_ERR_INVALID_ARG  # bad layout
+    assert libdas.das_permute(buf, ctypes.byref(buf, 32), 0, 1, 1, 1, 4, 4, 0, None) == das.DAS_ERR_INVALID_ARG  # bad layout
     assert libdas.das_permute(buf, ctypes.byref(buf, 32), 0, 1, 1, 1, 4, 0, 7, None) == das.DAS_ERR_INVALID_ARG  # bad storage
     # element alignment: float32 needs 4 bytes, complex64 8, a half copy 2
     base = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 16

@@ -49,7 +49,7 @@ def small_problems():
 @pytest.mark.parametrize("shape", [(32, 9, 16, 2048), (16, 3, 7, 100), (3, 2, 5, 37),
                                    (1, 1, 1, 1), (5, 1, 3, 64), (40, 2, 3, 33)])
 @pytest.mark.parametrize("dtype", ["f32", "c64"])
-@pytest.mark.parametrize("layout", [0, 1, 2])
+@pytest.mark.parametrize("layout", [0, 1, 2, 3])
 def test_permute_bit_exact(oracle, shape, dtype, layout):
     from volumetric_ultrasound_delay_gb300 import das
     rng = np.random.default_rng(zlib.crc32(repr((shape, dtype, layout)).encode()))
@@ -69,6 +69,16 @@ def test_permute_bit_exact(oracle, shape, dtype, layout):
         assert got[:, :, 1:K + 1].tobytes() == want.tobytes()
         pads = np.concatenate([got[:, :, :1], got[:, :, K + 1:]], axis=2)
         assert np.all(pads == np.asarray(7.5, dtype=x.dtype))
+        return
+    if layout == 3:
+        # padded planes: data planes 1..K, planes 0 and K + 1 left as they were
+        dst = torch.full(((K + 2) * Q * M * B,), 7.5, dtype=src.dtype, device="cuda")
+        das.permute(src, dst, layout)
+        torch.cuda.synchronize()
+        got = dst.cpu().numpy().reshape(K + 2, Q, M, B)
+        assert got[1:K + 1].tobytes() == oracle.permute(x, "kqmb").tobytes()
+        assert np.all(got[0] == np.asarray(7.5, dtype=x.dtype))
+        assert np.all(got[K + 1] == np.asarray(7.5, dtype=x.dtype))
         return
     dst = torch.empty_like(src).reshape(-1)
     das.permute(src, dst, layout)

@@ -65,11 +65,12 @@ struct das_plan_s {
     void *d_perm = nullptr;
     unsigned *d_flag = nullptr;               // set by the permute when the record holds NaN / inf
     size_t perm_bytes = 0;
-    bool perm_pads_zero = false;   // scratch holds the padded layout with zero pad rows
+    int perm_zero_layout = -1;     // padded layout (2 or 3) whose pad rows the scratch holds as zeros
     // device staging of das_beamform_host, and its copy stream / events
     void *d_rf = nullptr, *d_out = nullptr;
     float *d_tau = nullptr, *d_w = nullptr;
     int host_groups = 0;                      // DAS_OPT_HOST_GROUPS (0 = automatic)
+    int rx_groups = 1;                        // DAS_OPT_RX_GROUPS (0 = automatic)
     int storage = DAS_STORAGE_NATIVE;         // DAS_OPT_STORAGE
     cudaStream_t copy_stream = nullptr;
     std::vector<cudaEvent_t> copy_ev;         // [0]: start, [1]: tau/w copied, [2+g]: group g copied
@@ -145,6 +146,22 @@ std::vector<int> compact_order(const float *xyz, int N)
     for (int n = 0; n < N; ++n) order[n] = n;
     std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return key[a] < key[b]; });
     return order;
+}
+
+// Receiver groups of the brick kernel when DAS_OPT_RX_GROUPS is 0: enough that
+// one group's share of the permuted record fits in half of the L2.
+int auto_rx_groups(const das_plan_s *p)
+{
+    int l2 = 0, dev = p->device;
+    if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess || l2 <= 0) {
+        cudaGetLastError();
+        return 1;
+    }
+    const size_t elem = p->storage == DAS_STORAGE_F16 ? p->elem_bytes() / 2 : p->elem_bytes();
+    const size_t bytes = (size_t)p->B * p->Q * p->M * (p->K + 3) * elem;
+    const size_t share = (size_t)l2 / 2;
+    const size_t R = (bytes + share - 1) / share;
+    return R < 1 ? 1 : (R > 64 ? 64 : (int)R);
 }
 
 das_status check_supported(const das_plan_s *p, int kernel)
@@ -253,8 +270,9 @@ struct DoneMark {
     }
 };
 
-// Allocates the permute scratch on first use (sized for the padded layout, the
-// larger one) and zeroes it when the padded layout is about to be used after
+// Allocates the permute scratch on first use (sized for the brick kernel's
+// padded layout, the larger one) and zeroes it when a padded layout is about
+// to be used after
 // the scratch held something else; the permute never writes the pad rows.
 das_status ensure_scratch(das_plan_s *p, int layout, cudaStream_t stream)
 {
@@ -266,14 +284,13 @@ das_status ensure_scratch(das_plan_s *p, int layout, cudaStream_t stream)
         cudaError_t e = plan_alloc(p, &p->d_perm, p->padded_bytes());
         if (e != cudaSuccess) return cuda_fail(e, "permute scratch allocation");
         p->perm_bytes = p->padded_bytes();
-        p->perm_pads_zero = false;
+        p->perm_zero_layout = -1;
     }
-    if (layout == 2 && !p->perm_pads_zero) {
+    if (p->perm_zero_layout != layout) {
         cudaError_t e = cudaMemsetAsync(p->d_perm, 0, p->padded_bytes(), stream);
         if (e != cudaSuccess) return cuda_fail(e, "zeroing the permute scratch");
-        p->perm_pads_zero = true;
+        p->perm_zero_layout = layout;
     }
-    if (layout == 0) p->perm_pads_zero = false;
     return DAS_OK;
 }
 
@@ -502,8 +519,15 @@ das_status das_plan_set_option(das_plan p, int option, double value)
         const int v = (int)value;
         if ((double)v != value || (v != DAS_STORAGE_NATIVE && v != DAS_STORAGE_F16))
             return fail(DAS_ERR_INVALID_ARG, "storage must be DAS_STORAGE_NATIVE or DAS_STORAGE_F16");
-        if (v != p->storage) p->perm_pads_zero = false;   // pad rows move with the element size
+        if (v != p->storage) p->perm_zero_layout = -1;   // pad rows move with the element size
         p->storage = v;
+        return DAS_OK;
+    }
+    case DAS_OPT_RX_GROUPS: {
+        const int n = (int)value;
+        if ((double)n != value || n < 0 || n > 64)
+            return fail(DAS_ERR_INVALID_ARG, "receiver groups must be an integer in [0, 64]");
+        p->rx_groups = n;
         return DAS_OK;
     }
     case DAS_OPT_HOST_GROUPS: {
@@ -533,6 +557,7 @@ das_status das_plan_get_option(das_plan p, int option, double *value)
     case DAS_OPT_TIMING: *value = p->timing; return DAS_OK;
     case DAS_OPT_BI_GROUP: *value = p->bi_group; return DAS_OK;
     case DAS_OPT_HOST_GROUPS: *value = p->host_groups; return DAS_OK;
+    case DAS_OPT_RX_GROUPS: *value = p->rx_groups; return DAS_OK;
     case DAS_OPT_STORAGE: *value = p->storage; return DAS_OK;
     default: return fail(DAS_ERR_INVALID_ARG, "unknown option %d", option);
     }
@@ -563,7 +588,7 @@ das_status das_beamform(das_plan p, const void *rf, const float *tau_tx, const f
 
     const void *src = rf;
     const bool permute = kernel != DAS_KERNEL_BL;
-    const int layout = kernel == DAS_KERNEL_BI ? 0 : 2;
+    const int layout = kernel == DAS_KERNEL_BI ? 3 : 2;
     if (permute) {
         das_status st2 = ensure_scratch(p, layout, stream);
         if (st2 != DAS_OK) return st2;
@@ -595,9 +620,20 @@ das_status das_beamform(das_plan p, const void *rf, const float *tau_tx, const f
     case DAS_KERNEL_PAIR:
         e = das::launch_pair(p->geom, p->d_rx, src, tau_tx, w_tx, out, flag, stream);
         break;
-    default:
-        e = das::launch_brick(p->geom, p->d_rx, src, tau_tx, w_tx, out, cplx, stream, 0, -1, false, half);
+    default: {
+        // receivers in R launches of contiguous 32-receiver blocks, each adding
+        // to y: the launches' CTAs then read 1/R of the record at a time
+        const int blocks = (p->M + 31) / 32;
+        int R = p->rx_groups > 0 ? p->rx_groups : auto_rx_groups(p);
+        if (R > blocks) R = blocks;
+        for (int r = 0; r < R && e == cudaSuccess; ++r) {
+            const int m0 = 32 * (r * blocks / R);
+            const int m1 = std::min(p->M, 32 * ((r + 1) * blocks / R));
+            e = das::launch_brick(p->geom, p->d_rx, src, tau_tx, w_tx, out, cplx, stream, 0, -1,
+                                  r > 0, half, m0, m1);
+        }
         break;
+    }
     }
     if (e != cudaSuccess) return cuda_fail(e, "DAS kernel launch");
     if (p->timing) {
@@ -745,7 +781,7 @@ das_status das_permute(const void *in, void *out, das_dtype dtype, int B, int Q,
     if (dtype != DAS_F32 && dtype != DAS_C64) return fail(DAS_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
     if (B < 1 || Q < 1 || M < 1 || K < 1) return fail(DAS_ERR_INVALID_ARG, "B, Q, M, K must be >= 1");
     if ((long long)Q * M >= (1LL << 31)) return fail(DAS_ERR_INVALID_ARG, "Q*M must be < 2^31");
-    if (layout < 0 || layout > 2) return fail(DAS_ERR_INVALID_ARG, "layout must be 0, 1 or 2");
+    if (layout < 0 || layout > 3) return fail(DAS_ERR_INVALID_ARG, "layout must be 0, 1, 2 or 3");
     if (storage != DAS_STORAGE_NATIVE && storage != DAS_STORAGE_F16)
         return fail(DAS_ERR_INVALID_ARG, "unknown storage %d", (int)storage);
     const bool half = storage == DAS_STORAGE_F16;
@@ -755,7 +791,7 @@ das_status das_permute(const void *in, void *out, das_dtype dtype, int B, int Q,
     if ((reinterpret_cast<uintptr_t>(in) % eb) != 0 || (reinterpret_cast<uintptr_t>(out) % oeb) != 0)
         return fail(DAS_ERR_INVALID_ARG, "in and out must be aligned to their element sizes (%zu, %zu bytes)",
                     eb, oeb);
-    const size_t obytes = (size_t)B * Q * M * (K + (layout == 2 ? 3 : 0)) * oeb;
+    const size_t obytes = (size_t)B * Q * M * (K + (layout == 2 ? 3 : layout == 3 ? 2 : 0)) * oeb;
     const char *a = static_cast<const char *>(in);
     const char *b = static_cast<const char *>(out);
     if (a < b + obytes && b < a + bytes) return fail(DAS_ERR_INVALID_ARG, "in and out overlap");

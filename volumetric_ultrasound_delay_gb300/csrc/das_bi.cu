@@ -1,6 +1,9 @@
 // BI: batch-inner warp tiling (ffdas paper, Methods, batch-inner paragraphs
 // and Algorithm 2; ffdas docs, ALG2).  The record is first permuted to
-// K x Q x M x B so that b is contiguous.  A warp owns NW = 32 / G neighbouring
+// K x Q x M x B so that b is contiguous, here with a zero plane before k = 0
+// and one after k = K - 1 ((K+2) x Q x M x B, sample k at plane k + 1): a
+// pair that hangs over either end of the record reads a zero row, so every
+// pair reads planes k0 + 1 and k0 + 2 and needs no edge cases.  A warp owns NW = 32 / G neighbouring
 // voxels; the G lanes of a group share one voxel and split its frames: lane t
 // holds the 16-byte chunks t, t + G, t + 2G, ... of b, so at every (k, q, m)
 // the group reads G consecutive 16-byte vectors (full 32-byte sectors).
@@ -125,10 +128,16 @@ das_bi_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict__ 
             bool ok = false;
             if (ap) {
                 const float2 tw = txv[q];
-                const float wq = tw.y;
                 const float f = tw.x + d;
-                ok = sample_pair(f, wq, g.K, r0, w0, w1);
-                if (CPLX && ok) ph = demod_phase(g, f);
+                const float fl = floorf(f);
+                // a sample inside the record; false for NaN / inf
+                ok = fl >= -1.f && fl <= (float)(g.K - 1);
+                if (ok) {
+                    r0 = (int)fl + 1;                 // padded plane of sample k0
+                    w1 = tw.y * (f - fl);
+                    w0 = tw.y - w1;
+                    if (CPLX) ph = demod_phase(g, f);
+                }
             }
             // chunk index of the first row of this lane's pair
             const unsigned cidx = ok ? (unsigned)((long long)r0 * qmbc + ((long long)q * g.M + m) * bc) : 0u;
@@ -162,14 +171,14 @@ das_bi_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict__ 
                     W0[u] = CPLX ? make_float2(a0 * pj.x, a0 * pj.y) : make_float2(a0, a0);
                     W1[u] = CPLX ? make_float2(a1 * pj.x, a1 * pj.y) : make_float2(a1, a1);
                     const uint4 *p0 = perm4 + cj;
-                    // a row standing in for a sample outside the record is not read
-                    const bool r0_in = use[u] && !skip_row(a0), r1_in = use[u] && !skip_row(a1);
 #pragma unroll
                     for (int c = 0; c < J; ++c) {
                         v0[u][c] = make_uint4(0u, 0u, 0u, 0u);
                         v1[u][c] = v0[u][c];
-                        if (r0_in) v0[u][c] = __ldg(p0 + c * G);
-                        if (r1_in) v1[u][c] = __ldg(p0 + qmbc + c * G);
+                        if (use[u]) {
+                            v0[u][c] = __ldg(p0 + c * G);
+                            v1[u][c] = __ldg(p0 + qmbc + c * G);
+                        }
                     }
                 }
 #pragma unroll
@@ -254,8 +263,8 @@ bool choose(int B, bool cplx, bool half, int group, int &G, int &J)
 bool bi_supported(int B, bool cplx, int group, int Q, int M, int K, bool half)
 {
     int G, J;
-    // row indices travel as 32-bit counts of 16-byte chunks
-    const long long chunks = (long long)K * Q * M * B / (half ? (cplx ? 4 : 8) : (cplx ? 2 : 4));
+    // row indices travel as 32-bit counts of 16-byte chunks of the padded copy
+    const long long chunks = (long long)(K + 2) * Q * M * B / (half ? (cplx ? 4 : 8) : (cplx ? 2 : 4));
     return choose(B, cplx, half, group, G, J) && smem_bytes(G, Q) <= SMEM_MAX && chunks < (1LL << 32);
 }
 

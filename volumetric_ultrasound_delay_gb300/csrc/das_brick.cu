@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(THREADS, min_blocks<G, J, CPLX, HALF>())
 das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict__ perm,
                  const float *__restrict__ tau, const float *__restrict__ wtx,
                  float *__restrict__ out, int bricks_x, int bricks_y, int fb, int q_begin,
-                 int q_end, int add_to_out)
+                 int q_end, int m_begin, int m_end, int add_to_out)
 {
     using LY = Layout<G, J, CPLX, HALF, SPLIT>;
     constexpr int NW = 32 / G;                     // voxels per warp
@@ -314,7 +314,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
 #pragma unroll
         for (int e = 0; e < NP; ++e) acc[c][e] = make_float2(0.f, 0.f);
 
-    for (int m0 = 0; m0 < g.M; m0 += MC) {
+    for (int m0 = m_begin; m0 < m_end; m0 += MC) {
         // ---- phase A: distances of the warp's voxels to receiver m0 + lane
         const int m = m0 + lane;
         const RxPos r = m < g.M ? __ldg(rx + m) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -495,7 +495,8 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
 
 template <int G, int J, bool CPLX, bool HALF, bool SPLIT, bool WIDE>
 cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
-                       const float *w, void *out, cudaStream_t stream, int q0, int q1, bool acc)
+                       const float *w, void *out, cudaStream_t stream, int q0, int q1, int m0,
+                       int m1, bool acc)
 {
     constexpr int V = WARPS * (32 / G);
     constexpr int BX = BrickShape<V>::BX;
@@ -509,7 +510,7 @@ cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, cons
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     kernel<<<(int)blocks, THREADS, smem, stream>>>(g, rx, perm, tau, w, static_cast<float *>(out),
-                                                   bricks_x, bricks_y, fraction_bits(g.K), q0, q1,
+                                                   bricks_x, bricks_y, fraction_bits(g.K), q0, q1, m0, m1,
                                                    acc ? 1 : 0);
     return cudaGetLastError();
 }
@@ -565,16 +566,19 @@ bool brick_supported(int B, bool cplx, int K, bool half)
 
 cudaError_t launch_brick(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
                          const float *w, void *out, bool cplx, cudaStream_t stream, int q0, int q1,
-                         bool accumulate, bool half)
+                         bool accumulate, bool half, int m0, int m1)
 {
     int G, J;
     bool split;
     if (q1 < 0) q1 = g.Q;
+    if (m1 < 0) m1 = g.M;
     if (q0 < 0 || q0 > q1 || q1 > g.Q) return cudaErrorInvalidValue;
+    // receiver ranges start on a block of MC receivers
+    if (m0 < 0 || m0 > m1 || m1 > g.M || m0 % MC != 0) return cudaErrorInvalidValue;
     if (g.K < 2 || !choose(g.B, cplx, half, G, J, split)) return cudaErrorInvalidValue;
     // packed real entries while enough fraction bits remain, float entries beyond
     const bool wide = fraction_bits(g.K) < MIN_PACKED_BITS;
-#define DAS_BRICK_ARGS g, rx, perm, tau, w, out, stream, q0, q1, accumulate
+#define DAS_BRICK_ARGS g, rx, perm, tau, w, out, stream, q0, q1, m0, m1, accumulate
 #define DAS_BRICK_CASE(GG, JJ, HH, SS)                                                         \
     if (G == GG && J == JJ && half == HH && split == SS)                                       \
         return cplx ? launch_one<GG, JJ, true, HH, SS, false>(DAS_BRICK_ARGS)                  \

@@ -66,11 +66,13 @@ cudaError_t launch_bi(const DasGeom &g, const RxPos *rx, const void *perm, const
                       const float *w, void *out, bool cplx, int group, cudaStream_t stream,
                       bool half = false);
 bool brick_supported(int B, bool cplx, int K, bool half = false);
-// Sums transmits [q0, q1) (q1 < 0: all Q); with accumulate, adds to out
-// instead of overwriting it; half: perm holds half / half2 samples.
+// Sums transmits [q0, q1) (q1 < 0: all Q) and receivers [m0, m1) (m1 < 0: all
+// M; m0 a multiple of 32); with accumulate, adds to out instead of overwriting
+// it; half: perm holds half / half2 samples.
 cudaError_t launch_brick(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
                          const float *w, void *out, bool cplx, cudaStream_t stream, int q0 = 0,
-                         int q1 = -1, bool accumulate = false, bool half = false);
+                         int q1 = -1, bool accumulate = false, bool half = false, int m0 = 0,
+                         int m1 = -1);
 bool pair_supported(int B, bool cplx, int K, bool half = false);
 size_t pair_smem_bytes(int B, int Q);
 // float32 records; nonfinite: the flag the permute of this record set (the

@@ -44,6 +44,9 @@
 #ifndef DAS_PAIR_MIN_WARPS
 #define DAS_PAIR_MIN_WARPS 32
 #endif
+#ifndef DAS_PAIR_MIN_WARPS_J2
+#define DAS_PAIR_MIN_WARPS_J2 24
+#endif
 
 namespace das {
 namespace {
@@ -52,7 +55,8 @@ constexpr int MC = 32;                  // receivers per block (one per lane in 
 constexpr float FAR = 1.0e30f;          // distance marking "outside the aperture"
 constexpr int LIST_STRIDE = 2 * MC + 2; // up to two entries per receiver; 16-byte aligned lists
 
-// warp footprint: NP pairs, PX of them across x (two voxels each), the rest in y
+// warp footprint: NP pairs, two voxels each along x; BX voxels across x, the
+// rest in y
 template <int G>
 struct PairShape {
     static constexpr int NP = 32 / G;
@@ -61,6 +65,16 @@ struct PairShape {
     static constexpr int BY = V / BX;
     static_assert(V % BX == 0, "pairs tile the brick");
 };
+
+// shared memory of a CTA: the pairs' entry lists, the distances of phase A
+// (voxel-major, one per lane) and the voxels' transmit table
+template <int G>
+size_t smem_bytes(int Q)
+{
+    using SH = PairShape<G>;
+    return sizeof(uint2) * SH::NP * LIST_STRIDE + sizeof(float) * SH::V * MC +
+           sizeof(float2) * (size_t)SH::V * Q;
+}
 
 // Entry: x = row << 4 | pA << 3 | pB << 2 | dA << 1 | dB, with the window's
 // first row relative to the first row of the block of receivers, pX whether
@@ -87,17 +101,32 @@ __device__ __forceinline__ float2 fractions(unsigned y)
     return make_float2(a, b);
 }
 
+// J contiguous 16-byte chunks of a row (one 256-bit load for J = 2)
+template <int J>
+__device__ __forceinline__ void load_chunks(const char *p, uint4 (&v)[J])
+{
+    if constexpr (J == 2) {
+        asm("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+            : "=r"(v[0].x), "=r"(v[0].y), "=r"(v[0].z), "=r"(v[0].w),
+              "=r"(v[1].x), "=r"(v[1].y), "=r"(v[1].z), "=r"(v[1].w)
+            : "l"(p));
+    } else {
+#pragma unroll
+        for (int c = 0; c < J; ++c) v[c] = __ldg(reinterpret_cast<const uint4 *>(p) + c);
+    }
+}
+
 template <int U, int J>
 struct PTrip {
     uint2 e[U];
     uint4 s[U][3][J];
 };
 
-template <int G, int J>
-constexpr int min_blocks() { return DAS_PAIR_MIN_WARPS; }
+template <int J>
+constexpr int min_blocks() { return J == 1 ? DAS_PAIR_MIN_WARPS : DAS_PAIR_MIN_WARPS_J2; }
 
 template <int G, int J>
-__global__ void __launch_bounds__(32, min_blocks<G, J>())
+__global__ void __launch_bounds__(32, min_blocks<J>())
 das_pair_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict__ perm,
                 const float *__restrict__ tau, const float *__restrict__ wtx,
                 float *__restrict__ out, int bricks_x, int bricks_y, const unsigned *nonfinite,
@@ -105,12 +134,13 @@ das_pair_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict_
 {
     using SH = PairShape<G>;
     constexpr int NP = SH::NP, V = SH::V, BX = SH::BX;
-    constexpr int ROWB = 16 * G * J;
+    constexpr int ROWB = 16 * G * J;        // bytes per row: B float32 frames
     constexpr int U = DAS_PAIR_U;
 
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    uint2 *lists = reinterpret_cast<uint2 *>(smem_raw);                      // [2][NP][LIST_STRIDE]
-    float2 *tx = reinterpret_cast<float2 *>(lists + 2 * NP * LIST_STRIDE);   // [V][Q]
+    uint2 *lists = reinterpret_cast<uint2 *>(smem_raw);                     // [NP][LIST_STRIDE]
+    float *dist_s = reinterpret_cast<float *>(lists + NP * LIST_STRIDE);    // [V][32]
+    float2 *tx = reinterpret_cast<float2 *>(dist_s + V * MC);               // [V][Q]
     const int lane = threadIdx.x;
 
     const int bx = blockIdx.x % bricks_x;
@@ -151,10 +181,11 @@ das_pair_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict_
     __syncwarp();
 
     const int grp = lane / G;               // this group's pair: voxels 2 grp, 2 grp + 1
-    const int t = lane % G;
-    const char *permB = reinterpret_cast<const char *>(perm) + t * 16;
+    const int t = lane % G;                 // bytes [16 J t, 16 J (t + 1)) of every row
+    const char *permB = reinterpret_cast<const char *>(perm) + t * 16 * J;
     const unsigned below = (1u << lane) - 1u;
     const float kmax = (float)(g.K - 1);
+    const uint2 *ev = lists + grp * LIST_STRIDE;
 
     float2 accA[J][2], accB[J][2];
 #pragma unroll
@@ -169,35 +200,35 @@ das_pair_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict_
         for (int c = 0; c < J; ++c) ta.s[u][2][c] = tb.s[u][2][c] = make_uint4(0u, 0u, 0u, 0u);
 
     for (int m0 = 0; m0 < g.M; m0 += MC) {
-        // ---- phase A
+        // ---- phase A: distances of the warp's voxels to receiver m0 + lane
         const int m = m0 + lane;
         const RxPos r = m < g.M ? __ldg(rx + m) : make_float4(0.f, 0.f, 0.f, 0.f);
-        float dist[V];
         bool any = false;
-#pragma unroll
+#pragma unroll 4
         for (int i = 0; i < V; ++i) {
-            dist[i] = FAR;
+            float d = FAR;
             int n;
             float3 pos;
             if (m < g.M && voxel(i, n, &pos)) {
-                float d;
-                if (receive_geometry(g, pos, r, d)) {
-                    dist[i] = d;
+                float dd;
+                if (receive_geometry(g, pos, r, dd)) {
+                    d = dd;
                     any = true;
                 }
             }
+            dist_s[i * MC + lane] = d;
         }
         if (__ballot_sync(0xffffffffu, any) == 0u) continue;
 
         for (int q = q_begin; q < q_end; ++q) {
-            uint2 *lb = lists + (q & 1) * NP * LIST_STRIDE;
             const int base_row = (q * g.M + m0) * KP;
-            // ---- phase B
+            // ---- phase B: the pairs' entry lists (the previous transmit's
+            // phase C has finished reading them: __syncwarp below)
             int n_mine = 0;
-#pragma unroll
+#pragma unroll 2
             for (int p = 0; p < NP; ++p) {
-                const float fA = tx[(2 * p) * g.Q + q].x + dist[2 * p];
-                const float fB = tx[(2 * p + 1) * g.Q + q].x + dist[2 * p + 1];
+                const float fA = tx[(2 * p) * g.Q + q].x + dist_s[(2 * p) * MC + lane];
+                const float fB = tx[(2 * p + 1) * g.Q + q].x + dist_s[(2 * p + 1) * MC + lane];
                 const float flA = floorf(fA), flB = floorf(fB);
                 const bool okA = flA >= -1.f && flA <= kmax;    // false for NaN / inf / FAR
                 const bool okB = flB >= -1.f && flB <= kmax;
@@ -206,7 +237,7 @@ das_pair_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict_
                 const unsigned b1 = __ballot_sync(0xffffffffu, cnt >= 1);
                 const unsigned b2 = __ballot_sync(0xffffffffu, cnt >= 2);
                 if (cnt >= 1) {
-                    uint2 *L = lb + p * LIST_STRIDE + __popc(b1 & below) + __popc(b2 & below);
+                    uint2 *L = lists + p * LIST_STRIDE + __popc(b1 & below) + __popc(b2 & below);
                     if (both) {
                         const float k = fminf(flA, flB);
                         L[0] = make_entry(lane * KP + (int)k + 1, fA - k, fB - k, 12u);
@@ -224,7 +255,6 @@ das_pair_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict_
             // ---- phase C
             const float wqA = tx[(2 * grp) * g.Q + q].y;
             const float wqB = tx[(2 * grp + 1) * g.Q + q].y;
-            const uint2 *ev = lb + grp * LIST_STRIDE;
             auto row_ptr = [&](unsigned x) {
                 return permB + (long long)(base_row + (int)(x >> 4)) * ROWB;
             };
@@ -244,16 +274,14 @@ das_pair_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict_
                     }
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
-                        if (i + u >= n_mine) tr.e[u] = make_uint2(0u, 0x80008000u);
-                        if (i + u >= n_mine) continue;
-                        const char *p0 = row_ptr(tr.e[u].x);
-#pragma unroll
-                        for (int c = 0; c < J; ++c) {
-                            tr.s[u][0][c] = __ldg(reinterpret_cast<const uint4 *>(p0 + c * G * 16));
-                            tr.s[u][1][c] = __ldg(reinterpret_cast<const uint4 *>(p0 + ROWB + c * G * 16));
-                            if (tr.e[u].x & 3u)
-                                tr.s[u][2][c] = __ldg(reinterpret_cast<const uint4 *>(p0 + 2 * ROWB + c * G * 16));
+                        if (i + u >= n_mine) {
+                            tr.e[u] = make_uint2(0u, 0x80008000u);
+                            continue;
                         }
+                        const char *p0 = row_ptr(tr.e[u].x);
+                        load_chunks<J>(p0, tr.s[u][0]);
+                        load_chunks<J>(p0 + ROWB, tr.s[u][1]);
+                        if (tr.e[u].x & 3u) load_chunks<J>(p0 + 2 * ROWB, tr.s[u][2]);
                     }
                 };
                 auto use_trip = [&](const PTrip<U, J> &tr, int nu) {
@@ -266,12 +294,8 @@ das_pair_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict_
                         const float uA = wA * a.x, vA = wA - uA;
                         const float uB = wB * a.y, vB = wB - uB;
                         const bool dA = x & 2u, dB = x & 1u;
-                        const float2 cA0 = make_float2(dA ? 0.f : vA, dA ? 0.f : vA);
-                        const float2 cA1 = make_float2(dA ? vA : uA, dA ? vA : uA);
-                        const float2 cA2 = make_float2(dA ? uA : 0.f, dA ? uA : 0.f);
-                        const float2 cB0 = make_float2(dB ? 0.f : vB, dB ? 0.f : vB);
-                        const float2 cB1 = make_float2(dB ? vB : uB, dB ? vB : uB);
-                        const float2 cB2 = make_float2(dB ? uB : 0.f, dB ? uB : 0.f);
+                        const float cA0 = dA ? 0.f : vA, cA1 = dA ? vA : uA, cA2 = dA ? uA : 0.f;
+                        const float cB0 = dB ? 0.f : vB, cB1 = dB ? vB : uB, cB2 = dB ? uB : 0.f;
 #pragma unroll
                         for (int c = 0; c < J; ++c) {
 #pragma unroll
@@ -279,12 +303,12 @@ das_pair_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict_
                                 const float2 s0 = reinterpret_cast<const float2 *>(&tr.s[u][0][c])[h];
                                 const float2 s1 = reinterpret_cast<const float2 *>(&tr.s[u][1][c])[h];
                                 const float2 s2 = reinterpret_cast<const float2 *>(&tr.s[u][2][c])[h];
-                                accA[c][h] = __ffma2_rn(cA0, s0, accA[c][h]);
-                                accA[c][h] = __ffma2_rn(cA1, s1, accA[c][h]);
-                                accA[c][h] = __ffma2_rn(cA2, s2, accA[c][h]);
-                                accB[c][h] = __ffma2_rn(cB0, s0, accB[c][h]);
-                                accB[c][h] = __ffma2_rn(cB1, s1, accB[c][h]);
-                                accB[c][h] = __ffma2_rn(cB2, s2, accB[c][h]);
+                                accA[c][h] = __ffma2_rn(make_float2(cA0, cA0), s0, accA[c][h]);
+                                accA[c][h] = __ffma2_rn(make_float2(cA1, cA1), s1, accA[c][h]);
+                                accA[c][h] = __ffma2_rn(make_float2(cA2, cA2), s2, accA[c][h]);
+                                accB[c][h] = __ffma2_rn(make_float2(cB0, cB0), s0, accB[c][h]);
+                                accB[c][h] = __ffma2_rn(make_float2(cB1, cB1), s1, accB[c][h]);
+                                accB[c][h] = __ffma2_rn(make_float2(cB2, cB2), s2, accB[c][h]);
                             }
                         }
                     }
@@ -314,14 +338,15 @@ das_pair_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict_
                     const float w = isA ? wqA : wqB;
                     const float u1 = w * (isA ? a.x : a.y);
                     const float2 W0 = make_float2(w - u1, w - u1), W1 = make_float2(u1, u1);
+                    uint4 r0[J], r1[J];
+                    load_chunks<J>(p0, r0);
+                    load_chunks<J>(p0 + ROWB, r1);
 #pragma unroll
                     for (int c = 0; c < J; ++c) {
-                        const uint4 r0 = __ldg(reinterpret_cast<const uint4 *>(p0 + c * G * 16));
-                        const uint4 r1 = __ldg(reinterpret_cast<const uint4 *>(p0 + ROWB + c * G * 16));
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
-                            const float2 s0 = reinterpret_cast<const float2 *>(&r0)[h];
-                            const float2 s1 = reinterpret_cast<const float2 *>(&r1)[h];
+                            const float2 s0 = reinterpret_cast<const float2 *>(&r0[c])[h];
+                            const float2 s1 = reinterpret_cast<const float2 *>(&r1[c])[h];
                             float2 &acc = isA ? accA[c][h] : accB[c][h];
                             acc = __ffma2_rn(W1, s1, acc);
                             acc = __ffma2_rn(W0, s0, acc);
@@ -329,12 +354,12 @@ das_pair_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict_
                     }
                 }
             }
-            // the next transmit writes the other buffer; the one after that
-            // comes after the next __syncwarp
+            // the next transmit rewrites the lists
+            __syncwarp();
         }
     }
 
-    // ---- write-out: lane t holds frames 4 (t + c G) .. + 3 of both voxels
+    // ---- write-out: lane t holds frames 4 (J t + c) .. + 3 of both voxels
 #pragma unroll
     for (int vv = 0; vv < 2; ++vv) {
         int n;
@@ -345,7 +370,7 @@ das_pair_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict_
             for (int e = 0; e < 4; ++e) {
                 const float2 a2 = vv ? accB[c][e >> 1] : accA[c][e >> 1];
                 const float v = (e & 1) ? a2.y : a2.x;
-                float *o = out + (long long)((t + c * G) * 4 + e) * g.N + n;
+                float *o = out + (long long)((J * t + c) * 4 + e) * g.N + n;
                 *o = add_to_out ? *o + v : v;
             }
     }
@@ -361,7 +386,7 @@ cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, cons
     const int bricks_y = g.vox ? 1 : (g.ny + SH::BY - 1) / SH::BY;
     const long long blocks = (long long)bricks_x * bricks_y * (g.vox ? 1 : g.nz);
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    const size_t smem = sizeof(uint2) * 2 * SH::NP * LIST_STRIDE + sizeof(float2) * (size_t)SH::V * g.Q;
+    const size_t smem = smem_bytes<G>(g.Q);
     if (smem > 227 * 1024) return cudaErrorInvalidValue;
     auto kernel = das_pair_kernel<G, J>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -371,14 +396,20 @@ cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, cons
     return cudaGetLastError();
 }
 
-// lanes per pair for B float32 frames: one 16-byte chunk of the row per lane
+// lanes per pair G and 16-byte chunks per lane J for B float32 frames: a lane
+// holds 8 frames (one 256-bit load per row) where that leaves at least two
+// lanes per pair, else 4
 bool choose(int B, int &G, int &J)
 {
     if ((B * 4) % 16 != 0) return false;
     const int cpr = B * 4 / 16;
+#ifdef DAS_PAIR_FORCE_J1
     J = 1;
-    G = cpr;
-    return G == 4 || G == 8 || G == 16;
+#else
+    J = cpr >= 8 ? 2 : 1;
+#endif
+    G = cpr / J;
+    return (G == 4 || G == 8) && G * J == cpr;
 }
 
 }  // namespace
@@ -393,8 +424,11 @@ size_t pair_smem_bytes(int B, int Q)
 {
     int G, J;
     if (!choose(B, G, J)) return 0;
-    const int np = 32 / G;
-    return sizeof(uint2) * 2 * np * LIST_STRIDE + sizeof(float2) * (size_t)(2 * np) * Q;
+    switch (G) {
+    case 4: return smem_bytes<4>(Q);
+    case 8: return smem_bytes<8>(Q);
+    default: return smem_bytes<16>(Q);
+    }
 }
 
 cudaError_t launch_pair(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
@@ -406,12 +440,13 @@ cudaError_t launch_pair(const DasGeom &g, const RxPos *rx, const void *perm, con
     if (q0 < 0 || q0 > q1 || q1 > g.Q) return cudaErrorInvalidValue;
     if (g.K < 2 || !choose(g.B, G, J)) return cudaErrorInvalidValue;
     float *o = static_cast<float *>(out);
-    switch (G) {
-    case 4: return launch_one<4, 1>(g, rx, perm, tau, w, o, nonfinite, stream, q0, q1, accumulate);
-    case 8: return launch_one<8, 1>(g, rx, perm, tau, w, o, nonfinite, stream, q0, q1, accumulate);
-    case 16: return launch_one<16, 1>(g, rx, perm, tau, w, o, nonfinite, stream, q0, q1, accumulate);
-    default: return cudaErrorInvalidValue;
-    }
+#define DAS_PAIR_CASE(GG, JJ)                                                                   \
+    if (G == GG && J == JJ)                                                                     \
+        return launch_one<GG, JJ>(g, rx, perm, tau, w, o, nonfinite, stream, q0, q1, accumulate);
+    DAS_PAIR_CASE(4, 1) DAS_PAIR_CASE(8, 1)
+    DAS_PAIR_CASE(4, 2) DAS_PAIR_CASE(8, 2)
+#undef DAS_PAIR_CASE
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace das

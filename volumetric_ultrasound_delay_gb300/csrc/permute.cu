@@ -14,6 +14,10 @@
 //   layout 2: out[((q*M + m)*(K+3) + k + 1)*B + b] (Q x M x (K+3) x B: every
 //             (q, m) slab has a row before k = 0 and two rows after k = K-1
 //             that this kernel never writes; the brick kernel keeps them zero)
+//   layout 3: out[(((k+1)*Q + q)*M + m)*B + b]     ((K+2) x Q x M x B: the
+//             batch-inner layout with a plane before k = 0 and one after
+//             k = K-1 that this kernel never writes; the BI kernel keeps them
+//             zero)
 //
 // With half-precision storage the copy converts float32 -> half and complex64
 // -> half2 (round to nearest) as it writes: the pages' FP16 variants fuse that
@@ -160,10 +164,12 @@ cudaError_t launch_typed(const void *in, void *out, int B, int Q, int M, int K, 
     constexpr int V = 16 / sizeof(T);
     constexpr int VO = 16 / sizeof(TO);
     const int QM = Q * M;
-    const long long osk = layout == 0 ? (long long)QM * B : (long long)B;
-    const long long osqm = layout == 0 ? (long long)B
+    const bool kmajor = layout == 0 || layout == 3;
+    const long long osk = kmajor ? (long long)QM * B : (long long)B;
+    const long long osqm = kmajor ? (long long)B
                          : layout == 1 ? (long long)K * B : (long long)(K + 3) * B;
-    if (layout == 2) out = static_cast<TO *>(out) + B;   // row k = 0 of slab 0
+    if (layout == 2) out = static_cast<TO *>(out) + B;                      // row k = 0 of slab 0
+    if (layout == 3) out = static_cast<TO *>(out) + (long long)QM * B;      // plane k = 0
     const int blocks_b = (B + TILE - 1) / TILE;
     constexpr int SUB = sub_tiles<T>();
     const int blocks_k = (K + TILE * SUB - 1) / (TILE * SUB);

@@ -24,7 +24,8 @@ DAS_F32, DAS_C64, DAS_F64, DAS_C128 = 0, 1, 2, 3
 _DTYPES = {"f32": DAS_F32, "c64": DAS_C64, "f64": DAS_F64, "c128": DAS_C128}
 KERNELS = {"auto": 0, "bl": 1, "bi": 2, "brick": 3, "window": 4, "pair": 5}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
-OPT_KERNEL, OPT_DEMOD_HZ, OPT_TIMING, OPT_BI_GROUP, OPT_HOST_GROUPS, OPT_STORAGE = 0, 1, 2, 3, 4, 5
+OPT_KERNEL, OPT_DEMOD_HZ, OPT_TIMING, OPT_BI_GROUP, OPT_HOST_GROUPS, OPT_STORAGE, OPT_RX_GROUPS = \
+    0, 1, 2, 3, 4, 5, 6
 STORAGE_NATIVE, STORAGE_F16 = 0, 1
 
 # every function the header declares, with its ctypes signature
@@ -242,8 +243,10 @@ class Plan:
 
 
 def permute(rf, out, layout: int = 0, stream=None, storage: str = "native"):
-    """B x Q x M x K -> K x Q x M x B (layout 0), Q x M x K x B (layout 1) or
-    Q x M x (K+3) x B with sample k at row k + 1 and pad rows untouched (layout 2).
+    """B x Q x M x K -> K x Q x M x B (layout 0), Q x M x K x B (layout 1),
+    Q x M x (K+3) x B with sample k at row k + 1 and pad rows untouched (layout 2)
+    or (K+2) x Q x M x B with sample k at plane k + 1 and pad planes untouched
+    (layout 3).
     ``storage="native"`` copies bit for bit; ``"f16"`` writes float16 (float32 data)
     or complex32 as pairs of float16 (complex64 data), ``out`` being a float16
     tensor with 1 or 2 values per element."""
@@ -252,7 +255,7 @@ def permute(rf, out, layout: int = 0, stream=None, storage: str = "native"):
         raise TypeError("rf must be a 4-D float32 or complex64 CUDA tensor")
     B, Q, M, K = rf.shape
     dt = DAS_C64 if rf.dtype == torch.complex64 else DAS_F32
-    n_out = B * Q * M * (K + 3 if layout == 2 else K)
+    n_out = B * Q * M * (K + {2: 3, 3: 2}.get(layout, 0))
     if storage == "f16":
         n_out *= 2 if dt == DAS_C64 else 1
         optr = _dev_ptr(out, "out", torch.float16, n_out)
