@@ -62,6 +62,17 @@
 #ifndef DAS_BRICK_PACKED
 #define DAS_BRICK_PACKED 1     // real entries packed into 32 bits (else {row, fraction} floats)
 #endif
+// 4 lanes x 8 frames per voxel (one 256-bit load per row and lane) for rows of
+// 128 bytes, instead of 8 lanes x 4 frames; its warps per SM and trip size
+#ifndef DAS_BRICK_CONTIG_B32
+#define DAS_BRICK_CONTIG_B32 0
+#endif
+#ifndef DAS_BRICK_C_WARPS
+#define DAS_BRICK_C_WARPS 24
+#endif
+#ifndef DAS_BRICK_C_U
+#define DAS_BRICK_C_U 2
+#endif
 
 namespace das {
 namespace {
@@ -145,6 +156,14 @@ struct Trip {
     uint4 s[U][L];
 };
 
+// two adjacent 16-byte chunks in one 256-bit load
+__device__ __forceinline__ void load256(const char *p, uint4 &a, uint4 &b)
+{
+    asm("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+        : "l"(p));
+}
+
 // 16 bytes of samples -> NP float2 values: pairs of consecutive frames (real)
 // or one complex sample each (IQ), in float32
 template <bool HALF, int NP>
@@ -207,11 +226,18 @@ __device__ __forceinline__ void accumulate(float2 (&acc)[NA][NP], float wq, floa
 // they get fewer warps (more registers each); 16-lane groups (at most two
 // chunks a lane) fit 32 warps, 24 for complex with 4 entries per trip.  The
 // CTA count per SM is that over the warps per CTA.
+// A lane that holds its J chunks contiguously (4 lanes x 2 chunks: one 256-bit
+// load per row, so a group still reads one full 128-byte line per row).
+template <int G, int J, bool CPLX, bool HALF>
+constexpr bool contiguous_chunks() { return G == 4 && J == 2 && !CPLX && !HALF; }
+
 template <int G, int J, bool CPLX, bool HALF>
 constexpr int min_warps()
 {
-    return G == 16 ? (CPLX && J == 1 ? 24 : 32)
-                   : (J >= 4 ? 16 : (J == 2 || CPLX ? 24 : DAS_BRICK_MIN_WARPS));
+    return contiguous_chunks<G, J, CPLX, HALF>()
+               ? DAS_BRICK_C_WARPS
+               : G == 16 ? (CPLX && J == 1 ? 24 : 32)
+                         : (J >= 4 ? 16 : (J == 2 || CPLX ? 24 : DAS_BRICK_MIN_WARPS));
 }
 template <int G, int J, bool CPLX, bool HALF>
 constexpr int min_blocks()
@@ -223,8 +249,12 @@ constexpr int min_blocks()
 }
 
 // receivers per phase-C trip
-template <int J, bool HALF>
-constexpr int trip_size() { return J >= 4 ? 1 : (J == 2 ? 2 : DAS_BRICK_U1); }
+template <int G, int J, bool CPLX, bool HALF>
+constexpr int trip_size()
+{
+    return contiguous_chunks<G, J, CPLX, HALF>() ? DAS_BRICK_C_U
+                                                 : (J >= 4 ? 1 : (J == 2 ? 2 : DAS_BRICK_U1));
+}
 
 template <int G, int J, bool CPLX, bool HALF, bool SPLIT, bool WIDE>
 __global__ void __launch_bounds__(THREADS, min_blocks<G, J, CPLX, HALF>())
@@ -243,7 +273,8 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
     constexpr int NA = LY::NA;
     constexpr int ROWB = LY::ROWB;
     constexpr int CPR = ROWB / 16;                 // 16-byte chunks per row
-    constexpr int U = trip_size<J, HALF>();        // receivers per loop trip
+    constexpr int U = trip_size<G, J, CPLX, HALF>();   // receivers per loop trip
+    constexpr bool CONTIG = contiguous_chunks<G, J, CPLX, HALF>();
     constexpr int ES = entry_stride<CPLX>();
     using E = Entry<CPLX, HALF, WIDE>;
     constexpr bool PACKED = packed_entries<CPLX, HALF, WIDE>();
@@ -302,7 +333,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
     const int t = lane % G;
     // pair mode: load 2c + r of a lane is chunk t + G c of row r; split mode: the
     // lane's one load is chunk t of the row pair (row t / CPR)
-    const char *permB = reinterpret_cast<const char *>(perm) + t * 16;
+    const char *permB = reinterpret_cast<const char *>(perm) + t * 16 * (CONTIG ? J : 1);
     const int split_row = SPLIT ? t / CPR : 0;
     const unsigned below = (1u << lane) - 1u;
     const unsigned frac_mask = (1u << fb) - 1u;
@@ -389,7 +420,11 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                 // the L 16-byte loads of one entry
                 auto load_rows = [&](int row, uint4 (&s)[L]) {
                     const char *p0 = permB + (long long)row * ROWB;
-                    if constexpr (SPLIT) {
+                    if constexpr (CONTIG) {
+                        // chunks 2t, 2t + 1 of each row: s[2c + r] is chunk c of row r
+                        load256(p0, s[0], s[2]);
+                        load256(p0 + ROWB, s[1], s[3]);
+                    } else if constexpr (SPLIT) {
                         s[0] = __ldg(reinterpret_cast<const uint4 *>(p0));
                     } else {
 #pragma unroll
@@ -479,7 +514,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
     for (int c = 0; c < NA; ++c)
 #pragma unroll
         for (int e = 0; e < EPC; ++e) {
-            const int chunk = SPLIT ? t : t + c * G;
+            const int chunk = SPLIT ? t : (CONTIG ? J * t + c : t + c * G);
             const long long idx = (long long)(chunk * EPC + e) * g.N + n;
             if constexpr (CPLX) {
                 float2 *o = reinterpret_cast<float2 *>(out) + idx;
@@ -540,6 +575,11 @@ bool choose(int B, bool cplx, bool half, int &G, int &J, bool &split)
         J = cpr / 8;
         return cpr % 8 == 0 && (J == 1 || J == 2);
     }
+    if (cpr == 8 && !cplx && DAS_BRICK_CONTIG_B32) {
+        G = 4;          // 4 lanes x 8 frames, one 256-bit load per row and lane
+        J = 2;
+        return true;
+    }
     if (cpr <= 8) {
         G = cpr;
         J = 1;
@@ -589,7 +629,7 @@ cudaError_t launch_brick(const DasGeom &g, const RxPos *rx, const void *perm, co
                     : (wide ? launch_one<GG, JJ, false, false, false, true>(DAS_BRICK_ARGS)    \
                             : launch_one<GG, JJ, false, false, false, false>(DAS_BRICK_ARGS));
     DAS_BRICK_CASE_WIDE(2, 1) DAS_BRICK_CASE_WIDE(4, 1)
-    DAS_BRICK_CASE_WIDE(8, 1) DAS_BRICK_CASE_WIDE(8, 2)
+    DAS_BRICK_CASE_WIDE(8, 1) DAS_BRICK_CASE_WIDE(8, 2) DAS_BRICK_CASE_WIDE(4, 2)
     DAS_BRICK_CASE_WIDE(8, 4)
     DAS_BRICK_CASE_WIDE(16, 1) DAS_BRICK_CASE_WIDE(16, 2)
     DAS_BRICK_CASE(2, 1, true, true) DAS_BRICK_CASE(4, 1, true, true) DAS_BRICK_CASE(8, 1, true, true)

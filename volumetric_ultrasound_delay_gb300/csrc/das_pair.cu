@@ -45,7 +45,7 @@
 #define DAS_PAIR_MIN_WARPS 32
 #endif
 #ifndef DAS_PAIR_MIN_WARPS_J2
-#define DAS_PAIR_MIN_WARPS_J2 24
+#define DAS_PAIR_MIN_WARPS_J2 28
 #endif
 
 namespace das {

@@ -58,14 +58,14 @@ __device__ __forceinline__ __half convert<__half, float>(float v) { return __flo
 template <>
 __device__ __forceinline__ __half2 convert<__half2, float2>(float2 v) { return __float22half2_rn(v); }
 
-template <typename T, typename TO>
+// CHECK: also report non-finite float32 values (4- and 8-byte elements)
+template <typename T, typename TO, bool CHECK>
 __global__ void __launch_bounds__(THREADS)
 permute_kernel(const T *__restrict__ in, TO *__restrict__ out, int B, int QM, int K,
                long long osk, long long osqm, long long n_blocks, int blocks_b, int blocks_k,
                int vec_in, int vec_out, int qm0, unsigned *__restrict__ nonfinite)
 {
-    // float data (4- and 8-byte elements) can be checked for non-finite values
-    constexpr bool FLOATS = sizeof(T) % 4 == 0;
+    static_assert(!CHECK || sizeof(T) % 4 == 0, "only float data is checked");
     unsigned bad = 0u;
     constexpr int V = 16 / sizeof(T);            // input elements per 16-byte vector
     constexpr int VPR = TILE / V;                // input vectors per 32-element row
@@ -93,7 +93,7 @@ permute_kernel(const T *__restrict__ in, TO *__restrict__ out, int B, int QM, in
                     if (b < B && k < K) {   // K % V == 0, so the whole vector is inside
                         const uint4 u = __ldg(reinterpret_cast<const uint4 *>(
                             in + ((long long)b * QM + qm) * K + k));
-                        if (FLOATS && nonfinite)
+                        if constexpr (CHECK)
                             bad |= not_finite(u.x) | not_finite(u.y) | not_finite(u.z) | not_finite(u.w);
                         T vals[V];
                         memcpy(vals, &u, sizeof(u));
@@ -109,13 +109,11 @@ permute_kernel(const T *__restrict__ in, TO *__restrict__ out, int B, int QM, in
                     const int b = b0 + row, k = k0 + s * TILE + kk;
                     if (b < B && k < K) {
                         const T v = in[((long long)b * QM + qm) * K + k];
-                        if constexpr (FLOATS) {
-                            if (nonfinite) {
-                                unsigned w[sizeof(T) / 4];
-                                memcpy(w, &v, sizeof(T));
+                        if constexpr (CHECK) {
+                            unsigned w[sizeof(T) / 4];
+                            memcpy(w, &v, sizeof(T));
 #pragma unroll
-                                for (int j = 0; j < (int)(sizeof(T) / 4); ++j) bad |= not_finite(w[j]);
-                            }
+                            for (int j = 0; j < (int)(sizeof(T) / 4); ++j) bad |= not_finite(w[j]);
                         }
                         tile[s][row][kk] = v;
                     }
@@ -151,7 +149,7 @@ permute_kernel(const T *__restrict__ in, TO *__restrict__ out, int B, int QM, in
         }
         __syncthreads();
     }
-    if (nonfinite) {
+    if constexpr (CHECK) {
         const unsigned any = __ballot_sync(0xffffffffu, bad != 0u);
         if (any != 0u && (threadIdx.x & 31) == __ffs(any) - 1) atomicOr(nonfinite, 1u);
     }
@@ -181,9 +179,17 @@ cudaError_t launch_typed(const void *in, void *out, int B, int Q, int M, int K, 
     const int vec_out = out_al && (B % VO == 0) && (osk % VO == 0) && (osqm % VO == 0);
     const long long cap = (long long)num_sms * 8;
     const int grid = (int)(n_blocks < cap ? n_blocks : cap);
-    permute_kernel<T, TO><<<grid, THREADS, 0, stream>>>(
+    if constexpr (sizeof(T) % 4 == 0) {
+        if (nonfinite) {
+            permute_kernel<T, TO, true><<<grid, THREADS, 0, stream>>>(
+                static_cast<const T *>(in), static_cast<TO *>(out), B, QM, K, osk, osqm, n_blocks,
+                blocks_b, blocks_k, vec_in, vec_out, q0 * M, nonfinite);
+            return cudaGetLastError();
+        }
+    }
+    permute_kernel<T, TO, false><<<grid, THREADS, 0, stream>>>(
         static_cast<const T *>(in), static_cast<TO *>(out), B, QM, K, osk, osqm, n_blocks,
-        blocks_b, blocks_k, vec_in, vec_out, q0 * M, nonfinite);
+        blocks_b, blocks_k, vec_in, vec_out, q0 * M, nullptr);
     return cudaGetLastError();
 }
 
