@@ -242,9 +242,9 @@ cudaError_t plan_upload(das_plan_s *p, T **ptr, const void *src, size_t bytes)
 void release(das_plan_s *p)
 {
     if (p->own) {
-        if (p->used && p->done) cudaStreamWaitEvent(p->own, p->done, 0);
         void *bufs[] = {p->d_rx, p->d_vox, p->d_order, p->d_rx64, p->d_vox64,
                         p->d_perm, p->d_flag, p->d_rf, p->d_out, p->d_tau, p->d_w};
+        if (p->used && p->done) cudaStreamWaitEvent(p->own, p->done, 0);
         for (void *b : bufs)
             if (b) cudaFreeAsync(b, p->own);
     }

@@ -57,11 +57,14 @@ constexpr int LIST_STRIDE = 2 * MC + 2; // up to two entries per receiver; 16-by
 
 // warp footprint: NP pairs, two voxels each along x; BX voxels across x, the
 // rest in y
+#ifndef DAS_PAIR_BX
+#define DAS_PAIR_BX 4
+#endif
 template <int G>
 struct PairShape {
     static constexpr int NP = 32 / G;
     static constexpr int V = 2 * NP;
-    static constexpr int BX = NP >= 4 ? 4 : 2;
+    static constexpr int BX = V >= DAS_PAIR_BX ? DAS_PAIR_BX : 2;
     static constexpr int BY = V / BX;
     static_assert(V % BX == 0, "pairs tile the brick");
 };
