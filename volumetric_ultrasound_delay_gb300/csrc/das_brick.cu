@@ -33,14 +33,16 @@
 //            the warp's voxels is skipped;
 //   phase B (per transmit, lane = receiver): an entry for every pair that
 //            contributes (inside the voxel's aperture, a sample inside the
-//            record); a warp ballot compacts each voxel's entries into a dense
-//            list in the warp's own shared memory, and the list lengths stay in
-//            registers.  Lists are double-buffered by transmit parity (entry
-//            formats below);
+//            record), in aligned lists in the warp's own shared memory: a warp
+//            ballot over "some voxel of the warp contributes" gives each such
+//            receiver one slot in every voxel's list, so the groups read rows of
+//            the same slab in each instruction and share L1 lines; a voxel
+//            without a term for that receiver reads the slab's zero pad rows.
+//            Lists are double-buffered by transmit parity (entry formats below);
 //   phase C: each group walks its voxel's list U entries per trip, software
 //            pipelined: the row loads of the next trip are issued before the
 //            FMAs of the current one, so a warp keeps two trips of loads in
-//            flight; the groups of a warp run independently.  Real data are
+//            flight; with aligned lists the groups walk in step.  Real data are
 //            accumulated two frames at a time with the packed FP32 FMA of
 //            sm_100+ (__ffma2_rn), halving the FMA instructions.
 #include <cuda_fp16.h>
@@ -72,6 +74,14 @@
 #endif
 #ifndef DAS_BRICK_C_U
 #define DAS_BRICK_C_U 2
+#endif
+// aligned lists: slot s of every voxel's list belongs to the s-th receiver of
+// the block that contributes to some voxel of the warp, so the groups load rows
+// of one slab at the same time; where a voxel has no term for that receiver its
+// entry reads the slab's two zero pad rows (K+1, K+2) and adds exactly zero
+// (0: lists compacted per voxel, the form before)
+#ifndef DAS_BRICK_ALIGNED
+#define DAS_BRICK_ALIGNED 1
 #endif
 
 namespace das {
@@ -370,6 +380,43 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                 // ---- phase B: compacted entry lists of the warp's voxels
                 int n_mine = 0;
                 const int base_row = (q * g.M + m0) * KP;    // row 0 of this block's first slab
+                // the entry of voxel i for this lane's receiver
+                auto make = [&](float f, float fl) -> E {
+                    const int rel = lane * KP + (int)fl + 1;  // row within this block
+                    const float a = f - fl;                   // in [0, 1)
+                    if constexpr (CPLX) {
+                        const float2 ph = demod_phase(g, f);
+                        return make_float4(__int_as_float(base_row + rel), a, ph.x, ph.y);
+                    } else if constexpr (PACKED) {
+                        // fraction rounded to the nearest of its 2^fb steps, the last
+                        // step kept below 1 so the entry still reads rows k0 and
+                        // k0 + 1, the two samples the sum multiplies
+                        return ((unsigned)rel << fb) | min(__float2uint_rn(a * frac_scale), frac_mask);
+                    } else {
+                        return make_float2(__int_as_float(base_row + rel), a);
+                    }
+                };
+                if constexpr (DAS_BRICK_ALIGNED) {
+                    float fv[NW], flv[NW];
+                    bool okv[NW], any_v = false;
+#pragma unroll
+                    for (int i = 0; i < NW; ++i) {
+                        fv[i] = tx[(v0 + i) * g.Q + q].x + dist[i];
+                        flv[i] = floorf(fv[i]);
+                        okv[i] = (flv[i] >= -1.f) && (flv[i] <= (float)(g.K - 1));
+                        any_v |= okv[i];
+                    }
+                    const unsigned bal = __ballot_sync(0xffffffffu, any_v);
+                    if (any_v) {
+                        const int slot = __popc(bal & below);
+                        // no term: rows K+1 and K+2 of this lane's slab (pad rows, zero)
+                        const float pad = (float)g.K;
+#pragma unroll
+                        for (int i = 0; i < NW; ++i)
+                            eb[i * ES + slot] = okv[i] ? make(fv[i], flv[i]) : make(pad, pad);
+                    }
+                    n_mine = __popc(bal);
+                } else {
 #pragma unroll
                 for (int i = 0; i < NW; ++i) {
                     const float f = tx[(v0 + i) * g.Q + q].x + dist[i];
@@ -378,25 +425,9 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                     // record; false for NaN / inf
                     const bool ok = (fl >= -1.f) && (fl <= (float)(g.K - 1));
                     const unsigned bal = __ballot_sync(0xffffffffu, ok);
-                    if (ok) {
-                        const int rel = lane * KP + (int)fl + 1;  // row within this block
-                        const float a = f - fl;                   // in [0, 1)
-                        E e;
-                        if constexpr (CPLX) {
-                            const float2 ph = demod_phase(g, f);
-                            e = make_float4(__int_as_float(base_row + rel), a, ph.x, ph.y);
-                        } else if constexpr (PACKED) {
-                            // fraction rounded to the nearest of its 2^fb steps, the
-                            // last step kept below 1 so the entry still reads rows
-                            // k0 and k0 + 1, the two samples the sum multiplies
-                            e = ((unsigned)rel << fb) |
-                                min(__float2uint_rn(a * frac_scale), frac_mask);
-                        } else {
-                            e = make_float2(__int_as_float(base_row + rel), a);
-                        }
-                        eb[i * ES + __popc(bal & below)] = e;
-                    }
+                    if (ok) eb[i * ES + __popc(bal & below)] = make(f, fl);
                     if (i == grp) n_mine = __popc(bal);
+                }
                 }
                 __syncwarp();
 
