@@ -383,6 +383,28 @@ def test_two_plans_pipeline_volumes_on_two_streams(small_problems):
         assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("name", ["full_s", "iq_s", "large_s"])
+def test_receiver_groups_match_oracle(oracle, small_problems, name):
+    """DAS_OPT_RX_GROUPS splits the brick launch over blocks of 32 receivers,
+    each launch adding its receivers' terms to y: every split (one launch per
+    block, two, automatic) matches the oracle and the single launch up to the
+    float32 summation order."""
+    from volumetric_ultrasound_delay_gb300 import das
+    prob = small_problems[name]
+    ref, slack = oracle_beamform(oracle, prob)
+    inputs = device_inputs(prob)
+    ys = {}
+    for groups in (1, 2, 64, 0):
+        plan = plan_for(prob, "brick")
+        plan.set_option(das.OPT_RX_GROUPS, groups)
+        ys[groups] = plan.beamform(*inputs).cpu().numpy()
+        plan.close()
+        assert error_ratio(ys[groups], ref, slack) <= TOL, (name, groups)
+    peak = np.abs(ys[1]).max()
+    for groups in (2, 64, 0):
+        assert np.abs(ys[groups] - ys[1]).max() <= 1e-5 * peak, (name, groups)
+
+
 def test_timing_option_reports_both_kernels(small_problems):
     from volumetric_ultrasound_delay_gb300 import das
     prob = small_problems["full_s"]

@@ -93,10 +93,16 @@ constexpr int MC = 32;                 // receivers per block (one per lane in p
 constexpr float FAR = 1.0e30f;         // distance marking "outside the aperture"
 
 // brick footprint in x (voxels), as square as powers of two allow; the
-// footprint in y is V / BX
+// footprint in y is V / BX (DAS_BRICK_BX: a fixed footprint in x where it
+// divides V)
+#ifndef DAS_BRICK_BX
+#define DAS_BRICK_BX 0
+#endif
 template <int V>
 struct BrickShape {
-    static constexpr int BX = V >= 512 ? 32 : (V >= 128 ? 16 : (V >= 32 ? 8 : (V >= 4 ? 4 : V)));
+    static constexpr int BX = (DAS_BRICK_BX > 0 && V % (DAS_BRICK_BX > 0 ? DAS_BRICK_BX : 1) == 0)
+                                  ? (DAS_BRICK_BX > V ? V : DAS_BRICK_BX)
+                                  : (V >= 512 ? 32 : (V >= 128 ? 16 : (V >= 32 ? 8 : (V >= 4 ? 4 : V))));
     static_assert(V >= 1 && (V & (V - 1)) == 0 && V % BX == 0, "bricks tile V voxels");
 };
 
