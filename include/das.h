@@ -115,6 +115,19 @@ typedef enum {
                               (default) = one launch, 0 = enough launches for one share to
                               fit in half the L2.  Changes the float32 summation order,
                               not the result beyond it */
+    DAS_OPT_TX_GROUPS = 7, /* das_beamform with the brick kernel: number of launches the
+                              transmits are split into (contiguous ranges of transmits;
+                              each launch adds its transmits' terms to y), so the CTAs
+                              resident at one time read rows of fewer slabs and the rows
+                              they share stay in L2; 0 (default) = automatic: one launch
+                              when the permuted record holds less than one byte per 64
+                              accumulations (B*N*Q*M), else enough launches for one
+                              group's share of it to be at most 16 times the L2 size (2
+                              for 32 frames x 9 transmits x 1024 receivers x 2048 float32
+                              samples and 64^3 voxels on a 126 MB L2); 1 = one launch; at
+                              most Q launches are made.  Combines with
+                              DAS_OPT_RX_GROUPS (R x T launches).  Changes the float32
+                              summation order, not the result beyond it */
     DAS_OPT_HOST_GROUPS = 4 /* das_beamform_host with the brick or window kernel: number of transmit
                               groups the record is streamed in (copy of group g+1
                               overlapping the permute and sum of group g); 0 (default) =
@@ -205,6 +218,13 @@ das_status das_plan_get_option(das_plan plan, int option, double *value);
 
 /* The kernel das_beamform will run for this plan (after AUTO resolution). */
 das_status das_plan_kernel(das_plan plan, int *kernel);
+
+/* Kernel launches one das_beamform makes with the plan's current options: the
+ * permute (none for BL) plus the DAS launches (DAS_OPT_RX_GROUPS x
+ * DAS_OPT_TX_GROUPS for the brick kernel, else one).  No passage of the pages
+ * defines this call: it is library plumbing for profiling and accounting.
+ * Host only.  Errors: DAS_ERR_INVALID_ARG (NULL argument). */
+das_status das_plan_launches(das_plan plan, int *launches);
 
 /*
  * y = DAS(rf) on the device (the formula at the top of this file).

@@ -63,6 +63,7 @@ def test_host_side_rejections(libdas):
     # calls on a NULL plan
     assert libdas.das_beamform(None, None, None, None, None, None) == das.DAS_ERR_INVALID_ARG
     assert libdas.das_plan_set_option(None, 0, 0.0) == das.DAS_ERR_INVALID_ARG
+    assert libdas.das_plan_launches(None, None) == das.DAS_ERR_INVALID_ARG
     assert libdas.das_plan_destroy(None) == das.DAS_OK
     # permute argument checks
     assert libdas.das_permute(None, None, 0, 1, 1, 1, 1, 0, 0, None) == das.DAS_ERR_INVALID_ARG

@@ -58,5 +58,18 @@ def test_committed_traffic_record_names_its_commands():
     with open(bench.TRAFFIC_FILE) as f:
         rec = json.load(f)
     for key, r in rec.items():
-        assert r["dram_bytes_per_launch"] == r["dram_read"] + r["dram_write"], key
+        total = r.get("dram_bytes_per_call", r.get("dram_bytes_per_launch"))
+        assert total == r["dram_read"] + r["dram_write"], key
         assert r["command"].startswith("ncu ") and "--clock-control none" in r["command"], key
+        if "dram_bytes_per_call" in r:
+            # one capture of all the DAS launches of one call: -c equals the launch count
+            assert f"-c {r['launches_per_call']} " in r["command"], key
+
+
+def test_traffic_per_call_sums_the_launches(tmp_path, monkeypatch):
+    rec = {"brick/full": {"source_sha": bench.source_sha("brick"), "dram_bytes_per_call": 300,
+                          "launches_per_call": 2, "dram_read": 280, "dram_write": 20}}
+    path = tmp_path / "traffic.json"
+    path.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(path))
+    assert bench.measured_traffic("brick", "full") == 300

@@ -213,6 +213,11 @@ def test_unsupported_requests_are_rejected():
     plan = plan_for(prob)
     with pytest.raises(das.DasError):
         plan.set_option(das.OPT_DEMOD_HZ, 5e6)   # real plan cannot demodulate
+    for opt in (das.OPT_RX_GROUPS, das.OPT_TX_GROUPS):
+        for bad in (-1, 65, 1.5):
+            with pytest.raises(das.DasError) as exc:
+                plan.set_option(opt, bad)
+            assert exc.value.status == das.DAS_ERR_INVALID_ARG
     plan.close()
 
 
@@ -384,25 +389,31 @@ def test_two_plans_pipeline_volumes_on_two_streams(small_problems):
 
 
 @pytest.mark.parametrize("name", ["full_s", "iq_s", "large_s"])
-def test_receiver_groups_match_oracle(oracle, small_problems, name):
-    """DAS_OPT_RX_GROUPS splits the brick launch over blocks of 32 receivers,
-    each launch adding its receivers' terms to y: every split (one launch per
-    block, two, automatic) matches the oracle and the single launch up to the
-    float32 summation order."""
+def test_launch_groups_match_oracle(oracle, small_problems, name):
+    """DAS_OPT_RX_GROUPS and DAS_OPT_TX_GROUPS split the brick launch over
+    blocks of 32 receivers and ranges of transmits, each launch adding its
+    terms to y: every split (one launch per block or transmit, a few,
+    automatic) matches the oracle and the single launch up to the float32
+    summation order, and the plan reports the launches it makes."""
     from volumetric_ultrasound_delay_gb300 import das
     prob = small_problems[name]
     ref, slack = oracle_beamform(oracle, prob)
     inputs = device_inputs(prob)
+    splits = [(1, 1), (2, 1), (64, 1), (1, 2), (1, prob.Q), (2, 3), (0, 0)]
     ys = {}
-    for groups in (1, 2, 64, 0):
+    for rx, tx in splits:
         plan = plan_for(prob, "brick")
-        plan.set_option(das.OPT_RX_GROUPS, groups)
-        ys[groups] = plan.beamform(*inputs).cpu().numpy()
+        plan.set_option(das.OPT_RX_GROUPS, rx)
+        plan.set_option(das.OPT_TX_GROUPS, tx)
+        assert plan.get_option(das.OPT_TX_GROUPS) == tx
+        if rx > 0 and tx > 0:
+            assert plan.launches == 1 + min(rx, (prob.M + 31) // 32) * min(tx, prob.Q)
+        ys[rx, tx] = plan.beamform(*inputs).cpu().numpy()
         plan.close()
-        assert error_ratio(ys[groups], ref, slack) <= TOL, (name, groups)
-    peak = np.abs(ys[1]).max()
-    for groups in (2, 64, 0):
-        assert np.abs(ys[groups] - ys[1]).max() <= 1e-5 * peak, (name, groups)
+        assert error_ratio(ys[rx, tx], ref, slack) <= TOL, (name, rx, tx)
+    peak = np.abs(ys[1, 1]).max()
+    for key in splits[1:]:
+        assert np.abs(ys[key] - ys[1, 1]).max() <= 1e-5 * peak, (name, key)
 
 
 def test_timing_option_reports_both_kernels(small_problems):

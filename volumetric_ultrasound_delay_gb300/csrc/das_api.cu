@@ -71,6 +71,7 @@ struct das_plan_s {
     float *d_tau = nullptr, *d_w = nullptr;
     int host_groups = 0;                      // DAS_OPT_HOST_GROUPS (0 = automatic)
     int rx_groups = 1;                        // DAS_OPT_RX_GROUPS (0 = automatic)
+    int tx_groups = 0;                        // DAS_OPT_TX_GROUPS (0 = automatic)
     int storage = DAS_STORAGE_NATIVE;         // DAS_OPT_STORAGE
     cudaStream_t copy_stream = nullptr;
     std::vector<cudaEvent_t> copy_ev;         // [0]: start, [1]: tau/w copied, [2+g]: group g copied
@@ -162,6 +163,41 @@ int auto_rx_groups(const das_plan_s *p)
     const size_t share = (size_t)l2 / 2;
     const size_t R = (bytes + share - 1) / share;
     return R < 1 ? 1 : (R > 64 ? 64 : (int)R);
+}
+
+// Transmit groups of the brick kernel when DAS_OPT_TX_GROUPS is 0: enough that
+// one group's share of the permuted record is at most 16 times the L2.  The
+// CTAs resident at one time read a few hundred rows of every slab of their
+// group's transmits; with a share of that size those rows stay in L2 until the
+// neighbouring bricks that read them again have done so.  Each extra launch
+// repeats the receive distances, so the split is made only where the record's
+// re-reads weigh against the work: at least one byte of record per 64
+// accumulations (B N Q M); below that the kernel spends so long on each byte it
+// reads that DRAM re-reads cost nothing.
+int auto_tx_groups(const das_plan_s *p)
+{
+    int l2 = 0;
+    if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, p->device) != cudaSuccess || l2 <= 0) {
+        cudaGetLastError();
+        return 1;
+    }
+    const size_t elem = p->storage == DAS_STORAGE_F16 ? p->elem_bytes() / 2 : p->elem_bytes();
+    const size_t bytes = (size_t)p->B * p->Q * p->M * (p->K + 3) * elem;
+    const double accumulations = (double)p->B * (double)p->N * (double)p->Q * (double)p->M;
+    if ((double)bytes * 64.0 < accumulations) return 1;
+    const size_t share = (size_t)16 * (size_t)l2;
+    const size_t T = (bytes + share - 1) / share;
+    return T < 1 ? 1 : (T > (size_t)p->Q ? p->Q : (int)T);
+}
+
+// launches of the brick kernel in one das_beamform: receiver groups x transmit groups
+void brick_groups(const das_plan_s *p, int &R, int &T)
+{
+    const int blocks = (p->M + 31) / 32;
+    R = p->rx_groups > 0 ? p->rx_groups : auto_rx_groups(p);
+    if (R > blocks) R = blocks;
+    T = p->tx_groups > 0 ? p->tx_groups : auto_tx_groups(p);
+    if (T > p->Q) T = p->Q;
 }
 
 das_status check_supported(const das_plan_s *p, int kernel)
@@ -530,6 +566,13 @@ das_status das_plan_set_option(das_plan p, int option, double value)
         p->rx_groups = n;
         return DAS_OK;
     }
+    case DAS_OPT_TX_GROUPS: {
+        const int n = (int)value;
+        if ((double)n != value || n < 0 || n > 64)
+            return fail(DAS_ERR_INVALID_ARG, "transmit groups must be an integer in [0, 64]");
+        p->tx_groups = n;
+        return DAS_OK;
+    }
     case DAS_OPT_HOST_GROUPS: {
         const int n = (int)value;
         if ((double)n != value || n < 0 || n > 64)
@@ -558,6 +601,7 @@ das_status das_plan_get_option(das_plan p, int option, double *value)
     case DAS_OPT_BI_GROUP: *value = p->bi_group; return DAS_OK;
     case DAS_OPT_HOST_GROUPS: *value = p->host_groups; return DAS_OK;
     case DAS_OPT_RX_GROUPS: *value = p->rx_groups; return DAS_OK;
+    case DAS_OPT_TX_GROUPS: *value = p->tx_groups; return DAS_OK;
     case DAS_OPT_STORAGE: *value = p->storage; return DAS_OK;
     default: return fail(DAS_ERR_INVALID_ARG, "unknown option %d", option);
     }
@@ -567,6 +611,23 @@ das_status das_plan_kernel(das_plan p, int *kernel)
 {
     if (!p || !kernel) return fail(DAS_ERR_INVALID_ARG, "NULL argument");
     *kernel = resolve_kernel(p);
+    return DAS_OK;
+}
+
+das_status das_plan_launches(das_plan p, int *launches)
+{
+    if (!p || !launches) return fail(DAS_ERR_INVALID_ARG, "NULL argument");
+    const int kernel = resolve_kernel(p);
+    int n = kernel == DAS_KERNEL_BL ? 0 : 1;        // the permute
+    if (kernel == DAS_KERNEL_BRICK) {
+        DeviceGuard dg(p->device);
+        int R, T;
+        brick_groups(p, R, T);
+        n += R * T;
+    } else {
+        n += 1;
+    }
+    *launches = n;
     return DAS_OK;
 }
 
@@ -621,16 +682,18 @@ das_status das_beamform(das_plan p, const void *rf, const float *tau_tx, const f
         e = das::launch_pair(p->geom, p->d_rx, src, tau_tx, w_tx, out, flag, stream);
         break;
     default: {
-        // receivers in R launches of contiguous 32-receiver blocks, each adding
-        // to y: the launches' CTAs then read 1/R of the record at a time
+        // receivers in R launches of contiguous 32-receiver blocks and transmits
+        // in T launches of contiguous ranges, each launch adding to y: the
+        // launches' CTAs then read 1/(R T) of the record at a time
         const int blocks = (p->M + 31) / 32;
-        int R = p->rx_groups > 0 ? p->rx_groups : auto_rx_groups(p);
-        if (R > blocks) R = blocks;
+        int R, T;
+        brick_groups(p, R, T);
         for (int r = 0; r < R && e == cudaSuccess; ++r) {
             const int m0 = 32 * (r * blocks / R);
             const int m1 = std::min(p->M, 32 * ((r + 1) * blocks / R));
-            e = das::launch_brick(p->geom, p->d_rx, src, tau_tx, w_tx, out, cplx, stream, 0, -1,
-                                  r > 0, half, m0, m1);
+            for (int t = 0; t < T && e == cudaSuccess; ++t)
+                e = das::launch_brick(p->geom, p->d_rx, src, tau_tx, w_tx, out, cplx, stream,
+                                      t * p->Q / T, (t + 1) * p->Q / T, r > 0 || t > 0, half, m0, m1);
         }
         break;
     }

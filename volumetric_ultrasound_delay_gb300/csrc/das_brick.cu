@@ -83,6 +83,25 @@
 #ifndef DAS_BRICK_ALIGNED
 #define DAS_BRICK_ALIGNED 1
 #endif
+// rotated receiver loop: a brick starts its walk over the blocks of receivers
+// at the block the bricks resident with it have reached (percent of one wave
+// of resident CTAs per lap; 0: every brick starts at the first block)
+#ifndef DAS_BRICK_ROT
+#define DAS_BRICK_ROT 100
+#endif
+// complex64 rows of 64 frames (16 lanes x 2 chunks): two packed accumulators
+// per sample, one for the real and one for the imaginary part of the weight
+// (four packed FMAs per complex sample and entry instead of eight scalar ones;
+// 24 warps per SM for the registers); 0: complex FMAs.  Half2 storage keeps the
+// complex FMAs (fewer registers, more warps: faster there)
+#ifndef DAS_BRICK_CSPLIT
+#define DAS_BRICK_CSPLIT 1
+#endif
+// real float entries carry the weight w a of the second row instead of the
+// fraction a (phase B multiplies once per voxel and receiver, not each lane)
+#ifndef DAS_BRICK_WENTRY
+#define DAS_BRICK_WENTRY 1
+#endif
 
 namespace das {
 namespace {
@@ -207,13 +226,48 @@ __device__ __forceinline__ void mac(float2 &acc, float2 w, float2 s)
 // acc += w0 * (row-0 chunks) + w1 * (row-1 chunks), w1 = wq * fraction,
 // w0 = wq - w1 (IQ: both weights rotated by the entry's phase; real: the
 // weight broadcast to both frames of a pair).  In split mode the lane holds
-// one chunk of row `split_row`.
-template <bool CPLX, bool HALF, bool SPLIT, int NA, int NP, int L>
-__device__ __forceinline__ void accumulate(float2 (&acc)[NA][NP], float wq, float a, float2 ph,
+// one chunk of row `split_row`.  With split complex accumulators, acc[c][e]
+// collects w Re(ph) s and acc[c][NP + e] collects w Im(ph) s, each with
+// packed FMAs on (Re s, Im s); the output is the first plus i times the second.
+template <int G, int J, bool CPLX, bool HALF>
+constexpr bool split_complex() { return CPLX && !HALF && G == 16 && J == 2 && DAS_BRICK_CSPLIT != 0; }
+
+template <bool CPLX, bool HALF, bool SPLIT, bool PRE, bool CS, int NA, int NPA, int L>
+__device__ __forceinline__ void accumulate(float2 (&acc)[NA][NPA], float wq, float a, float2 ph,
                                            const uint4 (&s)[L], int split_row)
 {
-    const float w1 = wq * a;
+    constexpr int NP = CS ? NPA / 2 : NPA;
+    const float w1 = PRE ? a : wq * a;     // PRE: the entry holds w1 itself
     const float w0 = wq - w1;
+    if constexpr (CS) {
+        const float2 R0 = make_float2(w0 * ph.x, w0 * ph.x), I0 = make_float2(w0 * ph.y, w0 * ph.y);
+        const float2 R1 = make_float2(w1 * ph.x, w1 * ph.x), I1 = make_float2(w1 * ph.y, w1 * ph.y);
+        if constexpr (SPLIT) {
+            const float2 R = split_row ? R1 : R0, I = split_row ? I1 : I0;
+            float2 v[NP];
+            unpack<HALF, NP>(s[0], v);
+#pragma unroll
+            for (int e = 0; e < NP; ++e) {
+                acc[0][e] = __ffma2_rn(R, v[e], acc[0][e]);
+                acc[0][NP + e] = __ffma2_rn(I, v[e], acc[0][NP + e]);
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < NA; ++c) {
+                float2 v0[NP], v1[NP];
+                unpack<HALF, NP>(s[2 * c], v0);
+                unpack<HALF, NP>(s[2 * c + 1], v1);
+#pragma unroll
+                for (int e = 0; e < NP; ++e) {
+                    acc[c][e] = __ffma2_rn(R1, v1[e], acc[c][e]);
+                    acc[c][e] = __ffma2_rn(R0, v0[e], acc[c][e]);
+                    acc[c][NP + e] = __ffma2_rn(I1, v1[e], acc[c][NP + e]);
+                    acc[c][NP + e] = __ffma2_rn(I0, v0[e], acc[c][NP + e]);
+                }
+            }
+        }
+        return;
+    }
     const float2 W0 = CPLX ? make_float2(w0 * ph.x, w0 * ph.y) : make_float2(w0, w0);
     const float2 W1 = CPLX ? make_float2(w1 * ph.x, w1 * ph.y) : make_float2(w1, w1);
     if constexpr (SPLIT) {
@@ -247,12 +301,13 @@ __device__ __forceinline__ void accumulate(float2 (&acc)[NA][NP], float wq, floa
 template <int G, int J, bool CPLX, bool HALF>
 constexpr bool contiguous_chunks() { return G == 4 && J == 2 && !CPLX && !HALF; }
 
+// (split complex accumulators on 16 lanes x 2 chunks: 24 warps, 80 registers)
 template <int G, int J, bool CPLX, bool HALF>
 constexpr int min_warps()
 {
     return contiguous_chunks<G, J, CPLX, HALF>()
                ? DAS_BRICK_C_WARPS
-               : G == 16 ? (CPLX && J == 1 ? 24 : 32)
+               : G == 16 ? ((CPLX && J == 1) || split_complex<G, J, CPLX, HALF>() ? 24 : 32)
                          : (J >= 4 ? 16 : (J == 2 || CPLX ? 24 : DAS_BRICK_MIN_WARPS));
 }
 template <int G, int J, bool CPLX, bool HALF>
@@ -277,7 +332,7 @@ __global__ void __launch_bounds__(THREADS, min_blocks<G, J, CPLX, HALF>())
 das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict__ perm,
                  const float *__restrict__ tau, const float *__restrict__ wtx,
                  float *__restrict__ out, int bricks_x, int bricks_y, int fb, int q_begin,
-                 int q_end, int m_begin, int m_end, int add_to_out)
+                 int q_end, int m_begin, int m_end, int add_to_out, long long rot_wave)
 {
     using LY = Layout<G, J, CPLX, HALF, SPLIT>;
     constexpr int NW = 32 / G;                     // voxels per warp
@@ -294,6 +349,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
     constexpr int ES = entry_stride<CPLX>();
     using E = Entry<CPLX, HALF, WIDE>;
     constexpr bool PACKED = packed_entries<CPLX, HALF, WIDE>();
+    constexpr bool PRE = !CPLX && !PACKED && DAS_BRICK_WENTRY != 0;   // entries hold w a
 
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int tid = threadIdx.x;
@@ -355,13 +411,20 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
     const unsigned frac_mask = (1u << fb) - 1u;
     const float frac_scale = (float)(1u << fb);
 
-    float2 acc[NA][NP];
+    constexpr bool CS = split_complex<G, J, CPLX, HALF>();
+    constexpr int NPA = CS ? 2 * NP : NP;   // accumulators per chunk
+    float2 acc[NA][NPA];
 #pragma unroll
     for (int c = 0; c < NA; ++c)
 #pragma unroll
-        for (int e = 0; e < NP; ++e) acc[c][e] = make_float2(0.f, 0.f);
+        for (int e = 0; e < NPA; ++e) acc[c][e] = make_float2(0.f, 0.f);
 
-    for (int m0 = m_begin; m0 < m_end; m0 += MC) {
+    const int n_blocks = (m_end - m_begin + MC - 1) / MC;
+    const int b_first = rot_wave > 0 ? (int)(((long long)blockIdx.x * n_blocks / rot_wave) % n_blocks) : 0;
+    for (int bi = 0; bi < n_blocks; ++bi) {
+        int b = bi + b_first;
+        if (b >= n_blocks) b -= n_blocks;
+        const int m0 = m_begin + MC * b;
         // ---- phase A: distances of the warp's voxels to receiver m0 + lane
         const int m = m0 + lane;
         const RxPos r = m < g.M ? __ldg(rx + m) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -387,7 +450,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                 int n_mine = 0;
                 const int base_row = (q * g.M + m0) * KP;    // row 0 of this block's first slab
                 // the entry of voxel i for this lane's receiver
-                auto make = [&](float f, float fl) -> E {
+                auto make = [&](float f, float fl, float wv) -> E {
                     const int rel = lane * KP + (int)fl + 1;  // row within this block
                     const float a = f - fl;                   // in [0, 1)
                     if constexpr (CPLX) {
@@ -399,7 +462,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                         // k0 + 1, the two samples the sum multiplies
                         return ((unsigned)rel << fb) | min(__float2uint_rn(a * frac_scale), frac_mask);
                     } else {
-                        return make_float2(__int_as_float(base_row + rel), a);
+                        return make_float2(__int_as_float(base_row + rel), PRE ? wv * a : a);
                     }
                 };
                 if constexpr (DAS_BRICK_ALIGNED) {
@@ -419,7 +482,8 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                         const float pad = (float)g.K;
 #pragma unroll
                         for (int i = 0; i < NW; ++i)
-                            eb[i * ES + slot] = okv[i] ? make(fv[i], flv[i]) : make(pad, pad);
+                            eb[i * ES + slot] = okv[i] ? make(fv[i], flv[i], tx[(v0 + i) * g.Q + q].y)
+                                                    : make(pad, pad, 0.f);
                     }
                     n_mine = __popc(bal);
                 } else {
@@ -431,7 +495,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                     // record; false for NaN / inf
                     const bool ok = (fl >= -1.f) && (fl <= (float)(g.K - 1));
                     const unsigned bal = __ballot_sync(0xffffffffu, ok);
-                    if (ok) eb[i * ES + __popc(bal & below)] = make(f, fl);
+                    if (ok) eb[i * ES + __popc(bal & below)] = make(f, fl, tx[(v0 + i) * g.Q + q].y);
                     if (i == grp) n_mine = __popc(bal);
                 }
                 }
@@ -503,7 +567,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                 auto use_trip = [&](const Trip<U, L> &tr) {
 #pragma unroll
                     for (int u = 0; u < U; ++u)
-                        accumulate<CPLX, HALF, SPLIT>(acc, wq, tr.a[u], tr.ph[u], tr.s[u], split_row);
+                        accumulate<CPLX, HALF, SPLIT, PRE, CS>(acc, wq, tr.a[u], tr.ph[u], tr.s[u], split_row);
                 };
                 int i = 0;
                 if (n_mine >= U) {
@@ -528,7 +592,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                     uint4 s[L];
                     decode(ev[i], row, a, ph);
                     load_rows(row, s);
-                    accumulate<CPLX, HALF, SPLIT>(acc, wq, a, ph, s, split_row);
+                    accumulate<CPLX, HALF, SPLIT, PRE, CS>(acc, wq, a, ph, s, split_row);
                 }
                 // the next transmit writes the other buffer; the one after that
                 // comes after the next __syncwarp
@@ -539,7 +603,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
     if constexpr (SPLIT) {
         // add the row-1 half of each chunk (held CPR lanes further on) to row 0
 #pragma unroll
-        for (int e = 0; e < NP; ++e) {
+        for (int e = 0; e < NPA; ++e) {
             acc[0][e].x += __shfl_xor_sync(0xffffffffu, acc[0][e].x, CPR);
             acc[0][e].y += __shfl_xor_sync(0xffffffffu, acc[0][e].y, CPR);
         }
@@ -555,7 +619,10 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
             const long long idx = (long long)(chunk * EPC + e) * g.N + n;
             if constexpr (CPLX) {
                 float2 *o = reinterpret_cast<float2 *>(out) + idx;
-                const float2 v = acc[c][e];
+                const float2 v = CS
+                                     ? make_float2(acc[c][e].x - acc[c][NPA - NP + e].y,
+                                                   acc[c][e].y + acc[c][NPA - NP + e].x)
+                                     : acc[c][e];
                 *o = add_to_out ? make_float2(o->x + v.x, o->y + v.y) : v;
             } else {
                 float *o = out + idx;
@@ -581,9 +648,17 @@ cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, cons
     auto kernel = das_brick_kernel<G, J, CPLX, HALF, SPLIT, WIDE>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
+    // CTAs resident at once: the SMs times the CTAs per SM the launch bounds ask for
+    long long rot_wave = 0;
+    if (DAS_BRICK_ROT > 0) {
+        int dev = 0, sms = 0;
+        if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+        if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+        rot_wave = (long long)sms * min_blocks<G, J, CPLX, HALF>() * DAS_BRICK_ROT / 100;
+    }
     kernel<<<(int)blocks, THREADS, smem, stream>>>(g, rx, perm, tau, w, static_cast<float *>(out),
                                                    bricks_x, bricks_y, fraction_bits(g.K), q0, q1, m0, m1,
-                                                   acc ? 1 : 0);
+                                                   acc ? 1 : 0, rot_wave);
     return cudaGetLastError();
 }
 

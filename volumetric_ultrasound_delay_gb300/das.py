@@ -24,8 +24,8 @@ DAS_F32, DAS_C64, DAS_F64, DAS_C128 = 0, 1, 2, 3
 _DTYPES = {"f32": DAS_F32, "c64": DAS_C64, "f64": DAS_F64, "c128": DAS_C128}
 KERNELS = {"auto": 0, "bl": 1, "bi": 2, "brick": 3, "window": 4, "pair": 5}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
-OPT_KERNEL, OPT_DEMOD_HZ, OPT_TIMING, OPT_BI_GROUP, OPT_HOST_GROUPS, OPT_STORAGE, OPT_RX_GROUPS = \
-    0, 1, 2, 3, 4, 5, 6
+OPT_KERNEL, OPT_DEMOD_HZ, OPT_TIMING, OPT_BI_GROUP, OPT_HOST_GROUPS, OPT_STORAGE, OPT_RX_GROUPS, \
+    OPT_TX_GROUPS = 0, 1, 2, 3, 4, 5, 6, 7
 STORAGE_NATIVE, STORAGE_F16 = 0, 1
 
 # every function the header declares, with its ctypes signature
@@ -38,6 +38,7 @@ _SIGS = {
     "das_plan_set_option": (_I, [_VP, _I, ctypes.c_double]),
     "das_plan_get_option": (_I, [_VP, _I, ctypes.POINTER(ctypes.c_double)]),
     "das_plan_kernel": (_I, [_VP, ctypes.POINTER(_I)]),
+    "das_plan_launches": (_I, [_VP, ctypes.POINTER(_I)]),
     "das_beamform": (_I, [_VP, _VP, _VP, _VP, _VP, _VP]),
     "das_beamform_host": (_I, [_VP, _VP, _VP, _VP, _VP, _VP]),
     "das_plan_last_times": (_I, [_VP, ctypes.POINTER(_F), ctypes.POINTER(_F)]),
@@ -177,6 +178,13 @@ class Plan:
     @kernel.setter
     def kernel(self, name: str):
         self.set_option(OPT_KERNEL, KERNELS[name])
+
+    @property
+    def launches(self) -> int:
+        """Kernel launches one beamform call makes with the current options."""
+        n = ctypes.c_int()
+        _check(lib().das_plan_launches(self._h, ctypes.byref(n)))
+        return n.value
 
     # -- compute
     def _torch_dtypes(self):
