@@ -102,6 +102,11 @@
 #ifndef DAS_BRICK_WENTRY
 #define DAS_BRICK_WENTRY 1
 #endif
+// packed entries: the fraction decoded as 1 + a (a float in [1, 2)) and the
+// weight of the second row taken as wq (1 + a) - wq in one FMA
+#ifndef DAS_BRICK_FOLD
+#define DAS_BRICK_FOLD 1
+#endif
 
 namespace das {
 namespace {
@@ -232,12 +237,16 @@ __device__ __forceinline__ void mac(float2 &acc, float2 w, float2 s)
 template <int G, int J, bool CPLX, bool HALF>
 constexpr bool split_complex() { return CPLX && !HALF && G == 16 && J == 2 && DAS_BRICK_CSPLIT != 0; }
 
-template <bool CPLX, bool HALF, bool SPLIT, bool PRE, bool CS, int NA, int NPA, int L>
+// Weight of the second row from an entry's number a: WM 0, a is the fraction
+// (w1 = wq a); WM 1, a is w1 itself; WM 2, a is 1 + the fraction, so
+// w1 = wq (1 + fraction) - wq in one FMA, the same rounding of the same exact
+// product as wq * fraction.
+template <bool CPLX, bool HALF, bool SPLIT, int WM, bool CS, int NA, int NPA, int L>
 __device__ __forceinline__ void accumulate(float2 (&acc)[NA][NPA], float wq, float a, float2 ph,
                                            const uint4 (&s)[L], int split_row)
 {
     constexpr int NP = CS ? NPA / 2 : NPA;
-    const float w1 = PRE ? a : wq * a;     // PRE: the entry holds w1 itself
+    const float w1 = WM == 1 ? a : (WM == 2 ? fmaf(wq, a, -wq) : wq * a);
     const float w0 = wq - w1;
     if constexpr (CS) {
         const float2 R0 = make_float2(w0 * ph.x, w0 * ph.x), I0 = make_float2(w0 * ph.y, w0 * ph.y);
@@ -350,6 +359,8 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
     using E = Entry<CPLX, HALF, WIDE>;
     constexpr bool PACKED = packed_entries<CPLX, HALF, WIDE>();
     constexpr bool PRE = !CPLX && !PACKED && DAS_BRICK_WENTRY != 0;   // entries hold w a
+    constexpr bool FOLD = !CPLX && PACKED && DAS_BRICK_FOLD != 0;     // decode gives 1 + a
+    constexpr int WM = PRE ? 1 : (FOLD ? 2 : 0);
 
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int tid = threadIdx.x;
@@ -509,7 +520,8 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                     if constexpr (!CPLX && PACKED) {
                         row = base_row + (int)(e >> fb);
                         // fraction bits placed in a float mantissa of [1, 2), minus 1
-                        a = __int_as_float(0x3f800000 | ((e & frac_mask) << (23 - fb))) - 1.f;
+                        a = __int_as_float(0x3f800000 | ((e & frac_mask) << (23 - fb)));
+                        if constexpr (!FOLD) a -= 1.f;
                         ph = make_float2(1.f, 0.f);
                     } else {
                         row = __float_as_int(e.x);
@@ -567,7 +579,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                 auto use_trip = [&](const Trip<U, L> &tr) {
 #pragma unroll
                     for (int u = 0; u < U; ++u)
-                        accumulate<CPLX, HALF, SPLIT, PRE, CS>(acc, wq, tr.a[u], tr.ph[u], tr.s[u], split_row);
+                        accumulate<CPLX, HALF, SPLIT, WM, CS>(acc, wq, tr.a[u], tr.ph[u], tr.s[u], split_row);
                 };
                 int i = 0;
                 if (n_mine >= U) {
@@ -592,7 +604,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                     uint4 s[L];
                     decode(ev[i], row, a, ph);
                     load_rows(row, s);
-                    accumulate<CPLX, HALF, SPLIT, PRE, CS>(acc, wq, a, ph, s, split_row);
+                    accumulate<CPLX, HALF, SPLIT, WM, CS>(acc, wq, a, ph, s, split_row);
                 }
                 // the next transmit writes the other buffer; the one after that
                 // comes after the next __syncwarp
