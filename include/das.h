@@ -238,6 +238,10 @@ das_status das_plan_launches(das_plan plan, int *launches);
  * paper, Methods, batch-inner paragraph; ffdas docs, ALG2: permuted as part of
  * the launch), so one plan must not run two das_beamform calls at once; use one
  * plan per concurrent stream.
+ * The brick kernel on float32 records scales each transmit weight by at most
+ * 2^9 (an exact power of two) before forming the interpolation weights, so
+ * weights of magnitude above 2^119 (about 6.6e35) overflow there; every
+ * smaller weight gives the same float32 products as the unscaled arithmetic.
  * Errors: DAS_ERR_INVALID_ARG (null or misaligned pointers), DAS_ERR_UNSUPPORTED
  * (kernel cannot serve this plan), DAS_ERR_OUT_OF_MEMORY (scratch), DAS_ERR_CUDA
  * (launch failure).  Asynchronous.

@@ -416,6 +416,19 @@ def test_launch_groups_match_oracle(oracle, small_problems, name):
         assert np.abs(ys[key] - ys[1, 1]).max() <= 1e-5 * peak, (name, key)
 
 
+@pytest.mark.parametrize("kernel", ["brick", "bi", "bl"])
+def test_weights_scaled_by_a_power_of_two(small_problems, kernel):
+    """Scaling every transmit weight by 2^90 scales every product of the sum by
+    the same power of two, so y scales bit for bit: the brick kernel's weight
+    arithmetic (the weight scaled again by 2^(23 - fraction bits) inside) stays
+    exact far from float32's range limits."""
+    prob = small_problems["full_s"]
+    rf, tau, w = device_inputs(prob)
+    y1, _ = gpu_beamform(prob, kernel, inputs=(rf, tau, w))
+    y2, _ = gpu_beamform(prob, kernel, inputs=(rf, tau, w * 2.0 ** 90))
+    assert np.array_equal(y2, (y1.astype(np.float64) * 2.0 ** 90).astype(np.float32))
+
+
 def test_timing_option_reports_both_kernels(small_problems):
     from volumetric_ultrasound_delay_gb300 import das
     prob = small_problems["full_s"]

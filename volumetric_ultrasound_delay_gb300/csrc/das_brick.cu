@@ -107,6 +107,11 @@
 #ifndef DAS_BRICK_FOLD
 #define DAS_BRICK_FOLD 1
 #endif
+// packed entries: the fraction bits read in place as the low mantissa bits of
+// a float in [1, 2) (one masked OR), the transmit weight scaled by 2^(23 - fb)
+#ifndef DAS_BRICK_LOWFRAC
+#define DAS_BRICK_LOWFRAC 1
+#endif
 
 namespace das {
 namespace {
@@ -240,13 +245,14 @@ constexpr bool split_complex() { return CPLX && !HALF && G == 16 && J == 2 && DA
 // Weight of the second row from an entry's number a: WM 0, a is the fraction
 // (w1 = wq a); WM 1, a is w1 itself; WM 2, a is 1 + the fraction, so
 // w1 = wq (1 + fraction) - wq in one FMA, the same rounding of the same exact
-// product as wq * fraction.
+// product as wq * fraction; WM 3, a is 1 + the fraction's bits times 2^-23
+// and wqs = wq 2^(23 - fb), so w1 = wqs a - wqs, again the same product.
 template <bool CPLX, bool HALF, bool SPLIT, int WM, bool CS, int NA, int NPA, int L>
-__device__ __forceinline__ void accumulate(float2 (&acc)[NA][NPA], float wq, float a, float2 ph,
-                                           const uint4 (&s)[L], int split_row)
+__device__ __forceinline__ void accumulate(float2 (&acc)[NA][NPA], float wq, float wqs, float a,
+                                           float2 ph, const uint4 (&s)[L], int split_row)
 {
     constexpr int NP = CS ? NPA / 2 : NPA;
-    const float w1 = WM == 1 ? a : (WM == 2 ? fmaf(wq, a, -wq) : wq * a);
+    const float w1 = WM == 1 ? a : (WM == 2 ? fmaf(wq, a, -wq) : (WM == 3 ? fmaf(wqs, a, -wqs) : wq * a));
     const float w0 = wq - w1;
     if constexpr (CS) {
         const float2 R0 = make_float2(w0 * ph.x, w0 * ph.x), I0 = make_float2(w0 * ph.y, w0 * ph.y);
@@ -360,7 +366,8 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
     constexpr bool PACKED = packed_entries<CPLX, HALF, WIDE>();
     constexpr bool PRE = !CPLX && !PACKED && DAS_BRICK_WENTRY != 0;   // entries hold w a
     constexpr bool FOLD = !CPLX && PACKED && DAS_BRICK_FOLD != 0;     // decode gives 1 + a
-    constexpr int WM = PRE ? 1 : (FOLD ? 2 : 0);
+    constexpr bool LOWF = FOLD && DAS_BRICK_LOWFRAC != 0;            // fraction bits kept low
+    constexpr int WM = PRE ? 1 : (LOWF ? 3 : (FOLD ? 2 : 0));
 
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int tid = threadIdx.x;
@@ -421,6 +428,8 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
     const unsigned below = (1u << lane) - 1u;
     const unsigned frac_mask = (1u << fb) - 1u;
     const float frac_scale = (float)(1u << fb);
+    const unsigned frac_shift = 23u - (unsigned)fb;   // fraction bits -> top of a float mantissa
+    const float frac_pow = (float)(1u << frac_shift);
 
     constexpr bool CS = split_complex<G, J, CPLX, HALF>();
     constexpr int NPA = CS ? 2 * NP : NP;   // accumulators per chunk
@@ -514,25 +523,33 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
 
                 // ---- phase C: this group's list, U entries per trip, pipelined
                 const float wq = tx[(v0 + grp) * g.Q + q].y;
+                const float wqs = wq * frac_pow;               // (LOWF) wq 2^(23 - fb), exact
                 const E *ev = eb + grp * ES;
-                // entry -> row, fraction (and phase)
-                auto decode = [&](E e, int &row, float &a, float2 &ph) {
+                // first byte of this lane's chunk of the block's first row: packed
+                // entries give a row relative to it
+                const char *blk = permB + (long long)base_row * ROWB;
+                // entry -> address of the lane's chunk of its first row, fraction
+                // (and phase)
+                auto decode = [&](E e, const char *&row, float &a, float2 &ph) {
                     if constexpr (!CPLX && PACKED) {
-                        row = base_row + (int)(e >> fb);
-                        // fraction bits placed in a float mantissa of [1, 2), minus 1
-                        a = __int_as_float(0x3f800000 | ((e & frac_mask) << (23 - fb)));
+                        row = blk + (size_t)(e >> fb) * ROWB;
+                        // the fraction bits as the mantissa of a float in [1, 2): in
+                        // place as its low bits (LOWF: 1 + fraction 2^(fb - 23), the
+                        // weight scaled to match), or shifted to its top (the row bits
+                        // shift past the mantissa and are masked off)
+                        if constexpr (LOWF) a = __int_as_float((e & frac_mask) | 0x3f800000u);
+                        else a = __int_as_float(((e << frac_shift) & 0x007fffffu) | 0x3f800000u);
                         if constexpr (!FOLD) a -= 1.f;
                         ph = make_float2(1.f, 0.f);
                     } else {
-                        row = __float_as_int(e.x);
+                        row = permB + (long long)__float_as_int(e.x) * ROWB;
                         a = e.y;
                         if constexpr (CPLX) ph = make_float2(e.z, e.w);
                         else ph = make_float2(1.f, 0.f);
                     }
                 };
                 // the L 16-byte loads of one entry
-                auto load_rows = [&](int row, uint4 (&s)[L]) {
-                    const char *p0 = permB + (long long)row * ROWB;
+                auto load_rows = [&](const char *p0, uint4 (&s)[L]) {
                     if constexpr (CONTIG) {
                         // chunks 2t, 2t + 1 of each row: s[2c + r] is chunk c of row r
                         load256(p0, s[0], s[2]);
@@ -571,7 +588,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                     }
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
-                        int row;
+                        const char *row;
                         decode(e[u], row, tr.a[u], tr.ph[u]);
                         load_rows(row, tr.s[u]);
                     }
@@ -579,7 +596,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                 auto use_trip = [&](const Trip<U, L> &tr) {
 #pragma unroll
                     for (int u = 0; u < U; ++u)
-                        accumulate<CPLX, HALF, SPLIT, WM, CS>(acc, wq, tr.a[u], tr.ph[u], tr.s[u], split_row);
+                        accumulate<CPLX, HALF, SPLIT, WM, CS>(acc, wq, wqs, tr.a[u], tr.ph[u], tr.s[u], split_row);
                 };
                 int i = 0;
                 if (n_mine >= U) {
@@ -598,13 +615,13 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                     }
                 }
                 for (; i < n_mine; ++i) {
-                    int row;
+                    const char *row;
                     float a;
                     float2 ph;
                     uint4 s[L];
                     decode(ev[i], row, a, ph);
                     load_rows(row, s);
-                    accumulate<CPLX, HALF, SPLIT, WM, CS>(acc, wq, a, ph, s, split_row);
+                    accumulate<CPLX, HALF, SPLIT, WM, CS>(acc, wq, wqs, a, ph, s, split_row);
                 }
                 // the next transmit writes the other buffer; the one after that
                 // comes after the next __syncwarp
