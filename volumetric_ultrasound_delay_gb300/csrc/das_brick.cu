@@ -109,6 +109,11 @@
 #endif
 // packed entries: the fraction bits read in place as the low mantissa bits of
 // a float in [1, 2) (one masked OR), the transmit weight scaled by 2^(23 - fb)
+// complex entries carry the transmit weight times the demodulation phase, so
+// phase C forms the two complex weights with 2 multiplies and 2 subtractions
+#ifndef DAS_BRICK_IQPRE
+#define DAS_BRICK_IQPRE 0
+#endif
 #ifndef DAS_BRICK_LOWFRAC
 #define DAS_BRICK_LOWFRAC 1
 #endif
@@ -254,9 +259,13 @@ __device__ __forceinline__ void accumulate(float2 (&acc)[NA][NPA], float wq, flo
     constexpr int NP = CS ? NPA / 2 : NPA;
     const float w1 = WM == 1 ? a : (WM == 2 ? fmaf(wq, a, -wq) : (WM == 3 ? fmaf(wqs, a, -wqs) : wq * a));
     const float w0 = wq - w1;
+    // complex, WM 4: the entry's phase is already w exp(i phi), so the second
+    // row's complex weight is a times it and the first row's the rest
+    const float c1 = WM == 4 ? a * ph.x : w1 * ph.x, s1 = WM == 4 ? a * ph.y : w1 * ph.y;
+    const float c0 = WM == 4 ? ph.x - c1 : w0 * ph.x, s0 = WM == 4 ? ph.y - s1 : w0 * ph.y;
     if constexpr (CS) {
-        const float2 R0 = make_float2(w0 * ph.x, w0 * ph.x), I0 = make_float2(w0 * ph.y, w0 * ph.y);
-        const float2 R1 = make_float2(w1 * ph.x, w1 * ph.x), I1 = make_float2(w1 * ph.y, w1 * ph.y);
+        const float2 R0 = make_float2(c0, c0), I0 = make_float2(s0, s0);
+        const float2 R1 = make_float2(c1, c1), I1 = make_float2(s1, s1);
         if constexpr (SPLIT) {
             const float2 R = split_row ? R1 : R0, I = split_row ? I1 : I0;
             float2 v[NP];
@@ -283,8 +292,8 @@ __device__ __forceinline__ void accumulate(float2 (&acc)[NA][NPA], float wq, flo
         }
         return;
     }
-    const float2 W0 = CPLX ? make_float2(w0 * ph.x, w0 * ph.y) : make_float2(w0, w0);
-    const float2 W1 = CPLX ? make_float2(w1 * ph.x, w1 * ph.y) : make_float2(w1, w1);
+    const float2 W0 = CPLX ? make_float2(c0, s0) : make_float2(w0, w0);
+    const float2 W1 = CPLX ? make_float2(c1, s1) : make_float2(w1, w1);
     if constexpr (SPLIT) {
         const float2 W = split_row ? W1 : W0;
         float2 v[NP];
@@ -367,7 +376,8 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
     constexpr bool PRE = !CPLX && !PACKED && DAS_BRICK_WENTRY != 0;   // entries hold w a
     constexpr bool FOLD = !CPLX && PACKED && DAS_BRICK_FOLD != 0;     // decode gives 1 + a
     constexpr bool LOWF = FOLD && DAS_BRICK_LOWFRAC != 0;            // fraction bits kept low
-    constexpr int WM = PRE ? 1 : (LOWF ? 3 : (FOLD ? 2 : 0));
+    constexpr bool CPRE = CPLX && DAS_BRICK_IQPRE != 0;               // IQ entries hold w exp(i phi)
+    constexpr int WM = CPRE ? 4 : (PRE ? 1 : (LOWF ? 3 : (FOLD ? 2 : 0)));
 
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int tid = threadIdx.x;
@@ -475,7 +485,8 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
                     const float a = f - fl;                   // in [0, 1)
                     if constexpr (CPLX) {
                         const float2 ph = demod_phase(g, f);
-                        return make_float4(__int_as_float(base_row + rel), a, ph.x, ph.y);
+                        return CPRE ? make_float4(__int_as_float(base_row + rel), a, wv * ph.x, wv * ph.y)
+                                    : make_float4(__int_as_float(base_row + rel), a, ph.x, ph.y);
                     } else if constexpr (PACKED) {
                         // fraction rounded to the nearest of its 2^fb steps, the last
                         // step kept below 1 so the entry still reads rows k0 and
