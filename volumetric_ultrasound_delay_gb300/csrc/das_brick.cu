@@ -112,7 +112,7 @@
 // complex entries carry the transmit weight times the demodulation phase, so
 // phase C forms the two complex weights with 2 multiplies and 2 subtractions
 #ifndef DAS_BRICK_IQPRE
-#define DAS_BRICK_IQPRE 0
+#define DAS_BRICK_IQPRE 1
 #endif
 #ifndef DAS_BRICK_LOWFRAC
 #define DAS_BRICK_LOWFRAC 1
