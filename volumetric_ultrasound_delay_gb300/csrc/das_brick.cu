@@ -30,7 +30,10 @@
 //   phase A (per block of 32 receivers, lane = receiver): distance |x_v - r_m|
 //            in samples and the F-number test for the warp's NW voxels, kept in
 //            registers; a block whose receivers lie outside every aperture of
-//            the warp's voxels is skipped;
+//            the warp's voxels is skipped.  A brick starts its walk over the
+//            blocks at the one its co-resident bricks have reached (its CTA
+//            index over the CTAs resident at once), so that they spread over
+//            the record's slabs;
 //   phase B (per transmit, lane = receiver): an entry for every pair that
 //            contributes (inside the voxel's aperture, a sample inside the
 //            record), in aligned lists in the warp's own shared memory: a warp
@@ -44,7 +47,12 @@
 //            FMAs of the current one, so a warp keeps two trips of loads in
 //            flight; with aligned lists the groups walk in step.  Real data are
 //            accumulated two frames at a time with the packed FP32 FMA of
-//            sm_100+ (__ffma2_rn), halving the FMA instructions.
+//            sm_100+ (__ffma2_rn), halving the FMA instructions; the two rows'
+//            weights come from the entry with one FMA and one subtraction (the
+//            fraction read in place as mantissa bits, the transmit weight scaled
+//            to match), complex ones from the entry's weighted phase.
+// The host side may split the transmits (and the receivers) over several
+// launches that add to y, so that the record rows in use at one time fit L2.
 #include <cuda_fp16.h>
 
 #include "das_device.cuh"
