@@ -468,3 +468,28 @@ def test_full_size_sampled(oracle, name, samples):
         assert np.all(np.isfinite(y)) and np.abs(y).max() > 0
     del inputs
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name,storage,launches", [
+    ("full", "native", 3), ("full", "f16", 2), ("iq", "native", 4), ("iq", "f16", 3),
+    ("large", "native", 2), ("mid", "native", 2), ("tiny", "native", 2)])
+def test_automatic_transmit_groups(name, storage, launches):
+    """The automatic transmit split of the brick kernel on the five workloads:
+    one launch where the permuted record holds less than one byte per 64
+    accumulations (large) or fits 16 times the L2 (mid, tiny, half storage on
+    the full volume), else enough launches for a share of at most 16 times the
+    L2 (full: 2, IQ: 3, IQ half2: 2).  The plan reports the permute plus those
+    launches; no record is needed to ask."""
+    from volumetric_ultrasound_delay_gb300 import das, synth
+    wl = synth.workload(name)
+    grid = synth.grid_params(wl)
+    rx = synth.array_positions(wl.n_el).astype(np.float32)
+    props = torch.cuda.get_device_properties(0)
+    if not 101e6 <= props.L2_cache_size < 151e6:
+        pytest.skip("the counts above hold for an L2 of 101 to 151 MB")
+    plan = das.Plan(grid, rx, wl.c, wl.fs, wl.t0, wl.fnum, "c64" if wl.iq else "f32", wl.B, wl.Q, wl.M,
+                    wl.K, kernel="brick", f_demod=wl.f_demod, storage=storage)
+    assert plan.launches == launches
+    plan.set_option(das.OPT_TX_GROUPS, 1)
+    assert plan.launches == 2
+    plan.close()
