@@ -83,6 +83,10 @@ def parse_args():
                     help="override: voxel grid (for small profiling cases)")
     ap.add_argument("--storage", default="native", choices=["native", "f16"],
                     help="element type of the permuted record copy (f16: half precision)")
+    ap.add_argument("--record", default="native", choices=["native", "f16"],
+                    help="element type of the record the caller passes: native (float32 / "
+                         "complex64) or f16 (the synthetic record rounded to float16 / half2: "
+                         "DAS_F16 / DAS_C32H plans, half the bytes to copy and permute)")
     ap.add_argument("--host-groups", type=int, default=None,
                     help="e2e: transmit groups the host entry point streams the record in "
                          "(default: the library's automatic choice)")
@@ -361,9 +365,14 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     prob = make_workload(args)
-    dtype = "c64" if prob.wl.iq else "f32"
+    half_rec = args.record == "f16"
+    dtype = ("c32h" if half_rec else "c64") if prob.wl.iq else ("f16" if half_rec else "f32")
     A = prob.B * prob.N * prob.Q * prob.M
-    rf = torch.from_numpy(prob.rf).to(dev)
+    rf_src = torch.from_numpy(prob.rf)
+    if half_rec:
+        rf_src = rf_src.to(torch.complex32 if prob.wl.iq else torch.float16)
+    rf = rf_src.to(dev)
+    rec_bytes = rf.numel() * rf.element_size()
     tau = torch.from_numpy(prob.tau_tx).to(dev)
     w = torch.from_numpy(prob.w_tx).to(dev)
     out = torch.empty((prob.B, prob.N), dtype=torch.complex64 if prob.wl.iq else torch.float32,
@@ -385,7 +394,7 @@ def run_ours(args, world, rank, local):
     # a record smaller than twice the L2 could stay cached from one step to the
     # next: then a write of twice the L2 size runs between the timed steps
     l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or L2_FALLBACK)
-    flush = prob.rf.nbytes < 2 * l2_bytes
+    flush = rec_bytes < 2 * l2_bytes
     flush_buf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev) if flush else None
 
     sampler = ClockSampler(local)
@@ -417,14 +426,14 @@ def run_ours(args, world, rank, local):
     elapsed_ms = max_over_ranks(world, sum(step_ms) if flush else ev0.elapsed_time(ev1))
     ms_per_step = elapsed_ms / args.steps
     l2_note = (f"L2 flushed between steps (write of {2 * l2_bytes / 1e6:.0f} MB; "
-               f"{prob.rf.nbytes / 1e6:.0f} MB RF record), steps timed one by one" if flush else
-               f"inputs larger than L2 ({prob.rf.nbytes / 1e9:.2f} GB RF record), no flush")
+               f"{rec_bytes / 1e6:.0f} MB RF record), steps timed one by one" if flush else
+               f"inputs larger than L2 ({rec_bytes / 1e9:.2f} GB RF record), no flush")
     value = world * A / (ms_per_step / 1e3)
 
     # ---------------- e2e through the host entry point (pinned buffers)
     e2e = None
     if not args.no_e2e:
-        rf_h = torch.from_numpy(prob.rf).pin_memory()
+        rf_h = rf_src.pin_memory()
         tau_h = torch.from_numpy(prob.tau_tx).pin_memory()
         w_h = torch.from_numpy(prob.w_tx).pin_memory()
         out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -491,7 +500,7 @@ def run_ours(args, world, rank, local):
 
     # ---------------- every kernel on the same workload (the pages' relative figures)
     relative = None
-    if args.relative_steps > 0 and rank == 0:
+    if args.relative_steps > 0 and rank == 0 and not half_rec:
         plan.set_option(das.OPT_TIMING, 0)
         relative = relative_table(args, prob, rf, tau, w, out, stream, dev)
         plan.set_option(das.OPT_TIMING, 1)
@@ -548,7 +557,8 @@ def run_ours(args, world, rank, local):
     achieved = ISSUE_SLOTS_PER_ACC * A / (das_mean / 1e3) / 1e12
     achieved_in = ISSUE_SLOTS_PER_ACC * a_eff / (das_mean / 1e3) / 1e12
     # the captures were taken with the library's own launch split
-    traffic = measured_traffic(kernel, args.workload, args.storage) if args.tx_groups is None else None
+    traffic = (measured_traffic(kernel, args.workload, args.storage)
+               if args.tx_groups is None and args.record == "native" else None)
     roofline = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tinst/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "kernel": f"das_{kernel}_kernel", "kernel_ms": das_mean,
@@ -598,7 +608,7 @@ def run_ours(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "c64" if prob.wl.iq else "f32",
         "data": "synthetic (seeded numpy: N(0,1) noise + point-scatterer echoes)",
         "config": {"workload": describe(prob.wl), "kernel": kernel, "storage": args.storage,
-                   "launches_per_step": launches_per_call,
+                   "launches_per_step": launches_per_call, "record": args.record,
                    "accumulations_per_step": A,
                    "in_aperture_fraction": pairs / (prob.N * prob.M),
                    "l2": l2_note,

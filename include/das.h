@@ -60,7 +60,13 @@ typedef enum {
     DAS_C64 = 1,   /* interleaved complex64 IQ -> complex64 y */
     DAS_F64 = 2,   /* real float64 RF -> float64 y, computed in double; BL kernel only
                       (ffdas docs, ALG1 supports float64 and complex128) */
-    DAS_C128 = 3   /* interleaved complex128 IQ -> complex128 y, in double; BL only */
+    DAS_C128 = 3,  /* interleaved complex128 IQ -> complex128 y, in double; BL only */
+    DAS_F16 = 4,   /* real half-precision RF -> float32 y: the record as FP16 storage
+                      holds it (ffdas paper, Methods, FP16 paragraphs; ffdas docs,
+                      "Mixed-precision storage"), copied bit for bit by the permute and
+                      converted to float32 before interpolation; brick and BI kernels */
+    DAS_C32H = 5   /* interleaved half2 IQ (real, imaginary half precision) -> complex64
+                      y; as DAS_F16 */
 } das_dtype;
 
 /* Kernel choice (das_plan_set_option(DAS_OPT_KERNEL, ...)). */
@@ -172,8 +178,12 @@ typedef struct {
  *   c, fs    speed of sound (m/s) and sampling rate (Hz), both > 0.
  *   t0       time of sample 0 (seconds).
  *   fnum     receive F-number; <= 0 disables the aperture.
- *   dtype    DAS_F32, DAS_C64, DAS_F64 or DAS_C128 (the last two: BL kernel,
- *            double-precision geometry and arithmetic; tau_tx and w_tx stay float32).
+ *   dtype    DAS_F32, DAS_C64, DAS_F64 or DAS_C128 (these two: BL kernel,
+ *            double-precision geometry and arithmetic; tau_tx and w_tx stay
+ *            float32), DAS_F16 or DAS_C32H (brick and BI kernels; a record
+ *            already in half precision: half the bytes to copy and permute,
+ *            the same arithmetic as DAS_OPT_STORAGE = DAS_STORAGE_F16, which
+ *            is implied and may be set either way).
  *   B,Q,M,K  frames, transmits, receivers, samples per record (all >= 1);
  *            Q*M*(K+3) and B*N must stay below 2^31, K below 2^22.
  * Allocates the device copies of the geometry; the permute scratch of the BI,
@@ -297,7 +307,9 @@ das_status das_plan_destroy(das_plan plan);
  *             keeps them zero, so reads just outside the record return 0)
  *   layout 3: (K+2) x Q x M x B, sample k at plane k + 1; planes 0 and K + 1
  *             are not written (the BI kernel keeps them zero)
- *   in       device buffer of B*Q*M*K elements of dtype;
+ *   in       device buffer of B*Q*M*K elements of dtype (DAS_F32, DAS_C64,
+ *            DAS_F16 or DAS_C32H; the half types are copied bit for bit, with
+ *            either storage value);
  *   out      device buffer of B*Q*M*K (layouts 0, 1), B*Q*M*(K+3) (layout 2) or
  *            B*Q*M*(K+2) (layout 3)
  *            elements of dtype, or of half / half2 with DAS_STORAGE_F16; in and
@@ -334,7 +346,8 @@ das_status das_permute_bqmk_to_kqmb(const void *in, void *out, das_dtype dtype, 
  *
  * Arguments are those of das_plan_create and das_beamform together, except that
  *   rx_xyz   is a DEVICE pointer (M x 3 float32 receiver positions, metres), and
- *   f_demod  (Hz, DAS_C64 only; 0 = no rotation) is passed directly.
+ *   f_demod  (Hz, DAS_C64 only; 0 = no rotation) is passed directly, and
+ *   dtype    is DAS_F32 or DAS_C64 (other types: DAS_ERR_INVALID_ARG).
  * rf, tau_tx, w_tx and out are device buffers in the layouts of das_beamform.
  *
  * Scratch: one file-scope static device array of 64 MiB (67,108,864 bytes)

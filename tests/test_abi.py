@@ -64,6 +64,13 @@ def test_host_side_rejections(libdas):
     assert libdas.das_beamform(None, None, None, None, None, None) == das.DAS_ERR_INVALID_ARG
     assert libdas.das_plan_set_option(None, 0, 0.0) == das.DAS_ERR_INVALID_ARG
     assert libdas.das_plan_launches(None, None) == das.DAS_ERR_INVALID_ARG
+    # unknown dtypes; the half-precision records exist for plans and das_permute only
+    assert libdas.das_plan_create(ctypes.byref(h), ctypes.byref(g), rx, 1540.0, 20e6, 0.0, 1.5, 6, 1, 1, 1, 8) == das.DAS_ERR_INVALID_ARG
+    one = ctypes.create_string_buffer(1024)
+    for dtype in (das.DAS_F16, das.DAS_C32H, 6):
+        assert libdas.das_beamform_noalloc(ctypes.byref(g), one, 1540.0, 20e6, 0.0, 1.5, 0.0, dtype, 8, 1, 1, 8,
+                                           one, one, one, one, None) == das.DAS_ERR_INVALID_ARG
+        assert b"dtype" in libdas.das_last_error_string()
     assert libdas.das_plan_destroy(None) == das.DAS_OK
     # permute argument checks
     assert libdas.das_permute(None, None, 0, 1, 1, 1, 1, 0, 0, None) == das.DAS_ERR_INVALID_ARG
@@ -71,6 +78,9 @@ def test_host_side_rejections(libdas):
     assert libdas.das_permute(buf, buf, 0, 1, 1, 1, 4, 0, 0, None) == das.DAS_ERR_INVALID_ARG  # overlap
     assert libdas.das_permute(buf, ctypes.byref(buf, 32), 0, 1, 1, 1, 4, 4, 0, None) == das.DAS_ERR_INVALID_ARG  # bad layout
     assert libdas.das_permute(buf, ctypes.byref(buf, 32), 0, 1, 1, 1, 4, 0, 7, None) == das.DAS_ERR_INVALID_ARG  # bad storage
+    assert libdas.das_permute(buf, ctypes.byref(buf, 32), 6, 1, 1, 1, 4, 0, 0, None) == das.DAS_ERR_INVALID_ARG  # bad dtype
+    assert libdas.das_permute(buf, buf, das.DAS_F16, 1, 1, 1, 4, 0, 0, None) == das.DAS_ERR_INVALID_ARG  # overlap
+    assert libdas.das_permute(buf, ctypes.byref(buf, 32), das.DAS_F16, 1, 1, 1, 4, 4, 0, None) == das.DAS_ERR_INVALID_ARG  # layout
     # element alignment: float32 needs 4 bytes, complex64 8, a half copy 2
     base = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 16
     big = ctypes.create_string_buffer(256)

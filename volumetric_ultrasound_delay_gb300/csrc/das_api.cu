@@ -79,11 +79,32 @@ struct das_plan_s {
     DasGeom64 geom64{};
 
     bool is_double() const { return dtype == DAS_F64 || dtype == DAS_C128; }
-    bool is_complex() const { return dtype == DAS_C64 || dtype == DAS_C128; }
-    size_t elem_bytes() const { return dtype == DAS_C128 ? 16 : (dtype == DAS_F32 ? 4 : 8); }
+    bool is_complex() const { return dtype == DAS_C64 || dtype == DAS_C128 || dtype == DAS_C32H; }
+    // single-precision complex: complex64 or half2 samples, complex64 output
+    bool cplx32() const { return dtype == DAS_C64 || dtype == DAS_C32H; }
+    // the record arrives in half precision (DAS_F16, DAS_C32H)
+    bool half_in() const { return dtype == DAS_F16 || dtype == DAS_C32H; }
+    // the kernels read half-precision rows: half input, or float input stored as half
+    bool half_rows() const { return half_in() || storage == DAS_STORAGE_F16; }
+    // the permute rounds float32 / complex64 samples to half precision
+    bool convert_half() const { return !half_in() && storage == DAS_STORAGE_F16; }
+    // bytes of one record element as the caller passes it
+    size_t elem_bytes() const
+    {
+        switch (dtype) {
+        case DAS_F16: return 2;
+        case DAS_F32: case DAS_C32H: return 4;
+        case DAS_C128: return 16;
+        default: return 8;
+        }
+    }
+    // bytes of one element of the permuted copy the kernels read
+    size_t row_elem_bytes() const { return convert_half() ? elem_bytes() / 2 : elem_bytes(); }
+    // bytes of one output element (float32 / complex64 for the half inputs)
+    size_t out_elem_bytes() const { return dtype == DAS_F16 ? 4 : (dtype == DAS_C32H ? 8 : elem_bytes()); }
     size_t rf_bytes() const { return (size_t)B * Q * M * K * elem_bytes(); }
     size_t padded_bytes() const { return (size_t)B * Q * M * (K + 3) * elem_bytes(); }
-    size_t out_bytes() const { return (size_t)B * (size_t)N * elem_bytes(); }
+    size_t out_bytes() const { return (size_t)B * (size_t)N * out_elem_bytes(); }
     size_t txw_bytes() const { return (size_t)Q * (size_t)N * sizeof(float); }
 };
 
@@ -91,10 +112,10 @@ namespace {
 
 int resolve_kernel(const das_plan_s *p)
 {
-    const bool cplx = p->dtype == DAS_C64;
+    const bool cplx = p->cplx32();
     if (p->kernel != DAS_KERNEL_AUTO) return p->kernel;
     if (p->is_double()) return DAS_KERNEL_BL;                     // the only double-precision kernel
-    if (p->storage == DAS_STORAGE_F16) return DAS_KERNEL_BRICK;   // the only half-storage kernel
+    if (p->half_rows()) return DAS_KERNEL_BRICK;                  // half rows: brick (or BI on request)
     if (das::brick_supported(p->B, cplx, p->K)) return DAS_KERNEL_BRICK;
     if (p->K >= 2 && das::bi_supported(p->B, cplx, p->bi_group, p->Q, p->M, p->K)) return DAS_KERNEL_BI;
     return DAS_KERNEL_BL;
@@ -158,7 +179,7 @@ int auto_rx_groups(const das_plan_s *p)
         cudaGetLastError();
         return 1;
     }
-    const size_t elem = p->storage == DAS_STORAGE_F16 ? p->elem_bytes() / 2 : p->elem_bytes();
+    const size_t elem = p->row_elem_bytes();
     const size_t bytes = (size_t)p->B * p->Q * p->M * (p->K + 3) * elem;
     const size_t share = (size_t)l2 / 2;
     const size_t R = (bytes + share - 1) / share;
@@ -181,7 +202,7 @@ int auto_tx_groups(const das_plan_s *p)
         cudaGetLastError();
         return 1;
     }
-    const size_t elem = p->storage == DAS_STORAGE_F16 ? p->elem_bytes() / 2 : p->elem_bytes();
+    const size_t elem = p->row_elem_bytes();
     const size_t bytes = (size_t)p->B * p->Q * p->M * (p->K + 3) * elem;
     const double accumulations = (double)p->B * (double)p->N * (double)p->Q * (double)p->M;
     if ((double)bytes * 64.0 < accumulations) return 1;
@@ -202,10 +223,11 @@ void brick_groups(const das_plan_s *p, int &R, int &T)
 
 das_status check_supported(const das_plan_s *p, int kernel)
 {
-    const bool cplx = p->dtype == DAS_C64;
-    const bool half = p->storage == DAS_STORAGE_F16;
+    const bool cplx = p->cplx32();
+    const bool half = p->half_rows();
     if (half && kernel != DAS_KERNEL_BRICK && kernel != DAS_KERNEL_BI)
-        return fail(DAS_ERR_UNSUPPORTED, "half-precision storage is served by the brick and BI kernels only");
+        return fail(DAS_ERR_UNSUPPORTED,
+                    "half-precision records and storage are served by the brick and BI kernels only");
     if (p->is_double() && kernel != DAS_KERNEL_BL)
         return fail(DAS_ERR_UNSUPPORTED, "float64 / complex128 plans are served by the BL kernel only");
     switch (kernel) {
@@ -376,7 +398,7 @@ das_status das_plan_create(das_plan *plan, const das_grid *grid, const float *rx
     if (!(fs > 0.f) || !std::isfinite(fs)) return fail(DAS_ERR_INVALID_ARG, "fs must be > 0");
     if (!std::isfinite(t0) || !std::isfinite(fnum))
         return fail(DAS_ERR_INVALID_ARG, "t0 and fnum must be finite");
-    if (dtype < DAS_F32 || dtype > DAS_C128) return fail(DAS_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (dtype < DAS_F32 || dtype > DAS_C32H) return fail(DAS_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
     if (B < 1 || Q < 1 || M < 1 || K < 1) return fail(DAS_ERR_INVALID_ARG, "B, Q, M, K must be >= 1");
     const long long N = (long long)grid->nx * grid->ny * grid->nz;
     if ((long long)Q * M * (K + 3) >= (1LL << 31))
@@ -656,13 +678,14 @@ das_status das_beamform(das_plan p, const void *rf, const float *tau_tx, const f
     }
     cudaError_t e = cudaSuccess;
     if (p->timing) e = cudaEventRecord(p->ev[0], stream);
-    const bool half = p->storage == DAS_STORAGE_F16;
+    const bool half = p->half_rows();      // the kernels read half-precision rows
     // the pair kernel needs to know whether the record holds a non-finite sample
     unsigned *flag = kernel == DAS_KERNEL_PAIR ? p->d_flag : nullptr;
     if (e == cudaSuccess && flag) e = cudaMemsetAsync(flag, 0, sizeof(unsigned), stream);
     if (e == cudaSuccess && permute) {
+        // float input with half storage is rounded on the way; half input is copied
         e = das::launch_permute(rf, p->d_perm, (int)p->elem_bytes(), p->B, p->Q, p->M, p->K,
-                                layout, p->num_sms, stream, 0, -1, half, flag);
+                                layout, p->num_sms, stream, 0, -1, p->convert_half(), flag);
         src = p->d_perm;
     }
     if (e == cudaSuccess && p->timing) e = cudaEventRecord(p->ev[1], stream);
@@ -749,7 +772,7 @@ das_status das_beamform_host(das_plan p, const void *rf_host, const float *tau_t
             if (e != cudaSuccess) return cuda_fail(e, "copy events");
             p->copy_ev.push_back(ev);
         }
-        const bool cplx = p->dtype == DAS_C64;
+        const bool cplx = p->cplx32();
         const size_t eb = p->elem_bytes();
         const size_t plane = (size_t)p->M * p->K * eb;            // one transmit of one frame
         const size_t pitch = (size_t)p->Q * plane;                // one frame
@@ -775,10 +798,10 @@ das_status das_beamform_host(das_plan p, const void *rf_host, const float *tau_t
         for (int gi = 0; gi < groups && e == cudaSuccess; ++gi) {
             const int q0 = gi * p->Q / groups, q1 = (gi + 1) * p->Q / groups;
             e = cudaStreamWaitEvent(stream, p->copy_ev[2 + gi], 0);
-            const bool half = p->storage == DAS_STORAGE_F16;
+            const bool half = p->half_rows();
             if (e == cudaSuccess)
                 e = das::launch_permute(p->d_rf, p->d_perm, (int)eb, p->B, p->Q, p->M, p->K, 2,
-                                        p->num_sms, stream, q0, q1, half, flag);
+                                        p->num_sms, stream, q0, q1, p->convert_half(), flag);
             if (e == cudaSuccess)
                 e = kernel == DAS_KERNEL_WINDOW
                         ? das::launch_window(p->geom, p->d_rx, p->d_perm, p->d_tau, p->d_w, p->d_out,
@@ -841,14 +864,16 @@ das_status das_permute(const void *in, void *out, das_dtype dtype, int B, int Q,
                        int layout, das_storage storage, cudaStream_t stream)
 {
     if (!in || !out) return fail(DAS_ERR_INVALID_ARG, "NULL buffer");
-    if (dtype != DAS_F32 && dtype != DAS_C64) return fail(DAS_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (dtype != DAS_F32 && dtype != DAS_C64 && dtype != DAS_F16 && dtype != DAS_C32H)
+        return fail(DAS_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
     if (B < 1 || Q < 1 || M < 1 || K < 1) return fail(DAS_ERR_INVALID_ARG, "B, Q, M, K must be >= 1");
     if ((long long)Q * M >= (1LL << 31)) return fail(DAS_ERR_INVALID_ARG, "Q*M must be < 2^31");
     if (layout < 0 || layout > 3) return fail(DAS_ERR_INVALID_ARG, "layout must be 0, 1, 2 or 3");
     if (storage != DAS_STORAGE_NATIVE && storage != DAS_STORAGE_F16)
         return fail(DAS_ERR_INVALID_ARG, "unknown storage %d", (int)storage);
-    const bool half = storage == DAS_STORAGE_F16;
-    const size_t eb = dtype == DAS_C64 ? 8 : 4;
+    const bool half_in = dtype == DAS_F16 || dtype == DAS_C32H;
+    const bool half = storage == DAS_STORAGE_F16 && !half_in;      // round float samples to half
+    const size_t eb = dtype == DAS_C64 ? 8 : (dtype == DAS_F16 ? 2 : 4);
     const size_t bytes = (size_t)B * Q * M * K * eb;
     const size_t oeb = half ? eb / 2 : eb;
     if ((reinterpret_cast<uintptr_t>(in) % eb) != 0 || (reinterpret_cast<uintptr_t>(out) % oeb) != 0)
@@ -870,6 +895,7 @@ das_status das_permute(const void *in, void *out, das_dtype dtype, int B, int Q,
 das_status das_permute_bqmk_to_kqmb(const void *in, void *out, das_dtype dtype, int B, int Q, int M,
                                     int K, cudaStream_t stream)
 {
+    if (dtype != DAS_F32 && dtype != DAS_C64) return fail(DAS_ERR_INVALID_ARG, "dtype must be DAS_F32 or DAS_C64");
     return das_permute(in, out, dtype, B, Q, M, K, 0, DAS_STORAGE_NATIVE, stream);
 }
 

@@ -70,7 +70,7 @@ extern "C" das_status das_beamform_noalloc(const das_grid *grid, const float *rx
     const float gf[6] = {grid->x0, grid->y0, grid->z0, grid->dx, grid->dy, grid->dz};
     for (float v : gf)
         if (!std::isfinite(v)) return reject(DAS_ERR_INVALID_ARG, "grid origin/spacing not finite");
-    if (dtype != DAS_F32 && dtype != DAS_C64) return reject(DAS_ERR_INVALID_ARG, "unknown dtype");
+    if (dtype != DAS_F32 && dtype != DAS_C64) return reject(DAS_ERR_INVALID_ARG, "dtype must be DAS_F32 or DAS_C64");
     if (dtype == DAS_F32 && f_demod != 0.0)
         return reject(DAS_ERR_UNSUPPORTED, "demodulation needs DAS_C64 data");
     const bool cplx = dtype == DAS_C64;

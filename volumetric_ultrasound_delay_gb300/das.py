@@ -20,8 +20,9 @@ LIBRARY = Path(__file__).resolve().parent / "_lib" / "libdas.so"
 
 DAS_OK, DAS_ERR_INVALID_ARG, DAS_ERR_UNSUPPORTED, DAS_ERR_OUT_OF_MEMORY, DAS_ERR_CUDA, \
     DAS_ERR_TIMEOUT = range(6)
-DAS_F32, DAS_C64, DAS_F64, DAS_C128 = 0, 1, 2, 3
-_DTYPES = {"f32": DAS_F32, "c64": DAS_C64, "f64": DAS_F64, "c128": DAS_C128}
+DAS_F32, DAS_C64, DAS_F64, DAS_C128, DAS_F16, DAS_C32H = 0, 1, 2, 3, 4, 5
+_DTYPES = {"f32": DAS_F32, "c64": DAS_C64, "f64": DAS_F64, "c128": DAS_C128, "f16": DAS_F16,
+           "c32h": DAS_C32H}
 KERNELS = {"auto": 0, "bl": 1, "bi": 2, "brick": 3, "window": 4, "pair": 5}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 OPT_KERNEL, OPT_DEMOD_HZ, OPT_TIMING, OPT_BI_GROUP, OPT_HOST_GROUPS, OPT_STORAGE, OPT_RX_GROUPS, \
@@ -188,20 +189,24 @@ class Plan:
 
     # -- compute
     def _torch_dtypes(self):
+        """(float32, record dtype, output dtype): half records give float32 /
+        complex64 output."""
         import torch
-        return torch.float32, {"f32": torch.float32, "c64": torch.complex64,
-                               "f64": torch.float64, "c128": torch.complex128}[self.dtype]
+        rec = {"f32": torch.float32, "c64": torch.complex64, "f64": torch.float64,
+               "c128": torch.complex128, "f16": torch.float16, "c32h": torch.complex32}[self.dtype]
+        outd = {"f16": torch.float32, "c32h": torch.complex64}.get(self.dtype, rec)
+        return torch.float32, rec, outd
 
     def beamform(self, rf, tau_tx, w_tx, out=None, stream=None):
         """y (B x N) from device tensors rf (B x Q x M x K), tau_tx / w_tx (Q x N)."""
         import torch
-        f32, el = self._torch_dtypes()
+        f32, el, el_out = self._torch_dtypes()
         if out is None:
-            out = torch.empty((self.B, self.N), dtype=el, device=rf.device)
+            out = torch.empty((self.B, self.N), dtype=el_out, device=rf.device)
         _check(lib().das_beamform(
             self._h, _dev_ptr(rf, "rf", el, self.B * self.Q * self.M * self.K),
             _dev_ptr(tau_tx, "tau_tx", f32, self.Q * self.N), _dev_ptr(w_tx, "w_tx", f32, self.Q * self.N),
-            _dev_ptr(out, "out", el, self.B * self.N), _stream_handle(stream)))
+            _dev_ptr(out, "out", el_out, self.B * self.N), _stream_handle(stream)))
         return out
 
     def beamform_host(self, rf, tau_tx, w_tx, out, stream=None):
@@ -257,14 +262,17 @@ def permute(rf, out, layout: int = 0, stream=None, storage: str = "native"):
     (layout 3).
     ``storage="native"`` copies bit for bit; ``"f16"`` writes float16 (float32 data)
     or complex32 as pairs of float16 (complex64 data), ``out`` being a float16
-    tensor with 1 or 2 values per element."""
+    tensor with 1 or 2 values per element.  float16 and complex32 records are
+    copied bit for bit either way (``out`` of the record's dtype)."""
     import torch
-    if rf.dtype not in (torch.float32, torch.complex64) or rf.dim() != 4:
-        raise TypeError("rf must be a 4-D float32 or complex64 CUDA tensor")
+    dts = {torch.float32: DAS_F32, torch.complex64: DAS_C64, torch.float16: DAS_F16,
+           torch.complex32: DAS_C32H}
+    if rf.dtype not in dts or rf.dim() != 4:
+        raise TypeError("rf must be a 4-D float32, complex64, float16 or complex32 CUDA tensor")
     B, Q, M, K = rf.shape
-    dt = DAS_C64 if rf.dtype == torch.complex64 else DAS_F32
+    dt = dts[rf.dtype]
     n_out = B * Q * M * (K + {2: 3, 3: 2}.get(layout, 0))
-    if storage == "f16":
+    if storage == "f16" and dt in (DAS_F32, DAS_C64):
         n_out *= 2 if dt == DAS_C64 else 1
         optr = _dev_ptr(out, "out", torch.float16, n_out)
     else:
