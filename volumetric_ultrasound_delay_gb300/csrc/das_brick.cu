@@ -122,6 +122,15 @@
 #ifndef DAS_BRICK_IQPRE
 #define DAS_BRICK_IQPRE 1
 #endif
+// preferred shared-memory carveout in percent of the SM's unified L1 / shared
+// array (-1: the driver's choice).  44 % leaves about 128 KB of L1 while the
+// one-warp CTAs of the 32-frame float32 volume still fit 32 to an SM (each
+// holds its lists plus the 1 KB the runtime reserves per CTA): 11.19 ms there
+// against 11.41 with the driver's choice and 12.56 with 58 % or more, whose
+// smaller L1 misses more
+#ifndef DAS_BRICK_CARVEOUT
+#define DAS_BRICK_CARVEOUT 44
+#endif
 #ifndef DAS_BRICK_LOWFRAC
 #define DAS_BRICK_LOWFRAC 1
 #endif
@@ -696,6 +705,11 @@ cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, cons
     auto kernel = das_brick_kernel<G, J, CPLX, HALF, SPLIT, WIDE>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
+#if DAS_BRICK_CARVEOUT >= 0
+    // shared-memory share of the unified L1 / shared array the driver should prefer
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, DAS_BRICK_CARVEOUT);
+    if (err != cudaSuccess) return err;
+#endif
     // CTAs resident at once: the SMs times the CTAs per SM the launch bounds ask for
     long long rot_wave = 0;
     if (DAS_BRICK_ROT > 0) {
