@@ -343,22 +343,30 @@ template <int G, int J, bool CPLX, bool HALF>
 constexpr bool contiguous_chunks() { return G == 4 && J == 2 && !CPLX && !HALF; }
 
 // (split complex accumulators on 16 lanes x 2 chunks: 24 warps, 80 registers)
-template <int G, int J, bool CPLX, bool HALF>
+// MWO > 0 overrides the count: the 4-lane float32 layout runs at 28 warps (72
+// registers) when the record fits in L2 (16 frames, 5 x 256 slabs: 0.506 against
+// 0.516 ms; on records that stream from DRAM 28 warps lose 4 %)
+template <int G, int J, bool CPLX, bool HALF, int MWO = 0>
 constexpr int min_warps()
 {
-    return contiguous_chunks<G, J, CPLX, HALF>()
+    return MWO > 0 ? MWO
+         : contiguous_chunks<G, J, CPLX, HALF>()
                ? DAS_BRICK_C_WARPS
                : G == 16 ? ((CPLX && J == 1) || split_complex<G, J, CPLX, HALF>() ? 24 : 32)
                          : (J >= 4 ? 16 : (J == 2 || CPLX ? 24 : DAS_BRICK_MIN_WARPS));
 }
-template <int G, int J, bool CPLX, bool HALF>
+template <int G, int J, bool CPLX, bool HALF, int MWO = 0>
 constexpr int min_blocks()
 {
     // at least 1, at most the 32 resident CTAs an SM holds
-    return min_warps<G, J, CPLX, HALF>() / WARPS < 1
+    return min_warps<G, J, CPLX, HALF, MWO>() / WARPS < 1
                ? 1
-               : (min_warps<G, J, CPLX, HALF>() / WARPS > 32 ? 32 : min_warps<G, J, CPLX, HALF>() / WARPS);
+               : (min_warps<G, J, CPLX, HALF, MWO>() / WARPS > 32 ? 32
+                                                                  : min_warps<G, J, CPLX, HALF, MWO>() / WARPS);
 }
+#ifndef DAS_BRICK_L2_WARPS_G4
+#define DAS_BRICK_L2_WARPS_G4 28
+#endif
 
 // receivers per phase-C trip
 template <int G, int J, bool CPLX, bool HALF>
@@ -368,8 +376,8 @@ constexpr int trip_size()
                                                  : (J >= 4 ? 1 : (J == 2 ? 2 : DAS_BRICK_U1));
 }
 
-template <int G, int J, bool CPLX, bool HALF, bool SPLIT, bool WIDE>
-__global__ void __launch_bounds__(THREADS, min_blocks<G, J, CPLX, HALF>())
+template <int G, int J, bool CPLX, bool HALF, bool SPLIT, bool WIDE, int MWO>
+__global__ void __launch_bounds__(THREADS, min_blocks<G, J, CPLX, HALF, MWO>())
 das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict__ perm,
                  const float *__restrict__ tau, const float *__restrict__ wtx,
                  float *__restrict__ out, int bricks_x, int bricks_y, int fb, int q_begin,
@@ -689,7 +697,7 @@ das_brick_kernel(DasGeom g, const RxPos *__restrict__ rx, const void *__restrict
         }
 }
 
-template <int G, int J, bool CPLX, bool HALF, bool SPLIT, bool WIDE>
+template <int G, int J, bool CPLX, bool HALF, bool SPLIT, bool WIDE, int MWO = 0>
 cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, const float *tau,
                        const float *w, void *out, cudaStream_t stream, int q0, int q1, int m0,
                        int m1, bool acc)
@@ -702,21 +710,22 @@ cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, cons
     const long long blocks = (long long)bricks_x * bricks_y * (g.vox ? 1 : g.nz);
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     const size_t smem = smem_bytes<G, CPLX, HALF, WIDE>(g.Q);
-    auto kernel = das_brick_kernel<G, J, CPLX, HALF, SPLIT, WIDE>;
+    auto kernel = das_brick_kernel<G, J, CPLX, HALF, SPLIT, WIDE, MWO>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-#if DAS_BRICK_CARVEOUT >= 0
     // shared-memory share of the unified L1 / shared array the driver should prefer
-    err = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, DAS_BRICK_CARVEOUT);
-    if (err != cudaSuccess) return err;
-#endif
+    constexpr int carveout = DAS_BRICK_CARVEOUT;
+    if (carveout >= 0) {
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
+        if (err != cudaSuccess) return err;
+    }
     // CTAs resident at once: the SMs times the CTAs per SM the launch bounds ask for
     long long rot_wave = 0;
     if (DAS_BRICK_ROT > 0) {
         int dev = 0, sms = 0;
         if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
         if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
-        rot_wave = (long long)sms * min_blocks<G, J, CPLX, HALF>() * DAS_BRICK_ROT / 100;
+        rot_wave = (long long)sms * min_blocks<G, J, CPLX, HALF, MWO>() * DAS_BRICK_ROT / 100;
     }
     kernel<<<(int)blocks, THREADS, smem, stream>>>(g, rx, perm, tau, w, static_cast<float *>(out),
                                                    bricks_x, bricks_y, fraction_bits(g.K), q0, q1, m0, m1,
@@ -802,6 +811,17 @@ cudaError_t launch_brick(const DasGeom &g, const RxPos *rx, const void *perm, co
         return cplx ? launch_one<GG, JJ, true, false, false, false>(DAS_BRICK_ARGS)            \
                     : (wide ? launch_one<GG, JJ, false, false, false, true>(DAS_BRICK_ARGS)    \
                             : launch_one<GG, JJ, false, false, false, false>(DAS_BRICK_ARGS));
+    if (G == 4 && J == 1 && !cplx && !half && !split && !wide && DAS_BRICK_L2_WARPS_G4 > 0) {
+        // the 4-lane float32 layout with more registers a warp when the padded
+        // record fits in L2 (its loads then wait less and the extra registers
+        // keep more of them in flight)
+        int dev = 0, l2 = 0;
+        cudaError_t err = cudaGetDevice(&dev);
+        if (err == cudaSuccess) err = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+        if (err != cudaSuccess) return err;
+        if ((double)g.B * g.Q * g.M * (g.K + 3) * sizeof(float) <= (double)l2)
+            return launch_one<4, 1, false, false, false, false, DAS_BRICK_L2_WARPS_G4>(DAS_BRICK_ARGS);
+    }
     DAS_BRICK_CASE_WIDE(2, 1) DAS_BRICK_CASE_WIDE(4, 1)
     DAS_BRICK_CASE_WIDE(8, 1) DAS_BRICK_CASE_WIDE(8, 2) DAS_BRICK_CASE_WIDE(4, 2)
     DAS_BRICK_CASE_WIDE(8, 4)
