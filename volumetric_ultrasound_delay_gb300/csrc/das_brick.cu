@@ -55,6 +55,8 @@
 // launches that add to y, so that the record rows in use at one time fit L2.
 #include <cuda_fp16.h>
 
+#include <cmath>
+
 #include "das_device.cuh"
 
 // tuning (one chunk per lane, float32 or half storage): receivers per
@@ -123,11 +125,10 @@
 #define DAS_BRICK_IQPRE 1
 #endif
 // preferred shared-memory carveout in percent of the SM's unified L1 / shared
-// array (-1: the driver's choice).  44 % leaves about 128 KB of L1 while the
-// one-warp CTAs of the 32-frame float32 volume still fit 32 to an SM (each
-// holds its lists plus the 1 KB the runtime reserves per CTA): 11.19 ms there
-// against 11.41 with the driver's choice and 12.56 with 58 % or more, whose
-// smaller L1 misses more
+// array (-1: the driver's choice), raised where the CTAs the launch bounds ask
+// for need more.  Measured on the 32-frame float32 volume: 11.19 ms at 44 %
+// (a 200.7 KB shared configuration, by the profiler) against 11.41 ms with the
+// driver's choice (102.4 KB) and 12.56 ms at 58 % or more
 #ifndef DAS_BRICK_CARVEOUT
 #define DAS_BRICK_CARVEOUT 44
 #endif
@@ -713,9 +714,20 @@ cudaError_t launch_one(const DasGeom &g, const RxPos *rx, const void *perm, cons
     auto kernel = das_brick_kernel<G, J, CPLX, HALF, SPLIT, WIDE, MWO>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    // shared-memory share of the unified L1 / shared array the driver should prefer
-    constexpr int carveout = DAS_BRICK_CARVEOUT;
-    if (carveout >= 0) {
+    // shared-memory share of the unified L1 / shared array the driver should
+    // prefer: DAS_BRICK_CARVEOUT, or more where the CTAs the launch bounds ask
+    // for need more (lists of float entries, long transmit tables)
+    if (DAS_BRICK_CARVEOUT >= 0) {
+        int dev = 0, per_sm = 0, reserved = 0;
+        if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+        if ((err = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess)
+            return err;
+        if ((err = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess)
+            return err;
+        const double need = (double)min_blocks<G, J, CPLX, HALF, MWO>() * (double)(smem + reserved);
+        int carveout = per_sm > 0 ? (int)std::ceil(100.0 * need / per_sm) : 100;
+        if (carveout < DAS_BRICK_CARVEOUT) carveout = DAS_BRICK_CARVEOUT;
+        if (carveout > 100) carveout = 100;
         err = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
         if (err != cudaSuccess) return err;
     }
