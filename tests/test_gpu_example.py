@@ -1,5 +1,5 @@
-"""The usage example of the Python binding (volumetric_ultrasound_delay_gb300/example.py,
-the code README.md shows) runs as written."""
+"""The usage example of the Python binding (volumetric_ultrasound_delay_gb300/example.py)
+runs as written."""
 import pytest
 
 pytestmark = pytest.mark.gpu
