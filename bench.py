@@ -70,6 +70,8 @@ def parse_args():
     ap.add_argument("--workload", default="full", choices=["tiny", "mid", "full", "iq", "large"])
     ap.add_argument("--kernel", default="auto", choices=["auto", "bl", "bi", "brick", "window", "pair"])
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-volumes", type=int, default=3,
+                    help="e2e.stream: volumes per das_beamform_host_volumes call (0 = skip)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -457,6 +459,26 @@ def run_ours(args, world, rank, local):
         ref = out.cpu()
         if float((out_h - ref).abs().max()) > 1e-5 * float(ref.abs().max()):
             raise RuntimeError("host entry point disagrees with the device entry point")
+        if args.e2e_volumes > 0:
+            # a stream of volumes through one call: each volume's record copied
+            # and its y read back inside the timed region
+            nv = args.e2e_volumes
+            rf_v = torch.empty((nv,) + tuple(rf_src.shape), dtype=rf_src.dtype).pin_memory()
+            rf_v.copy_(rf_src.unsqueeze(0).expand_as(rf_v))
+            out_v = torch.empty((nv,) + tuple(out.shape), dtype=out.dtype).pin_memory()
+            plan.beamform_host_volumes(rf_v, tau_h, w_h, out_v, stream=stream)      # warm-up
+            barrier(world)
+            t = time.perf_counter()
+            plan.beamform_host_volumes(rf_v, tau_h, w_h, out_v, stream=stream)
+            vol_s = max_over_ranks(world, time.perf_counter() - t)
+            if float((out_v[-1] - ref).abs().max()) > 1e-5 * float(ref.abs().max()):
+                raise RuntimeError("volume stream disagrees with the device entry point")
+            e2e["stream"] = {"volumes": nv, "ms_per_volume": 1e3 * vol_s / nv,
+                             "value": world * A * nv / vol_s, "unit": UNIT,
+                             "h2d_bytes_per_volume": e2e["h2d_bytes_per_step"] - int(2 * tau_h.numel() * 4),
+                             "note": "das_beamform_host_volumes: one call, one plan; each volume's record "
+                                     "copied and its y read back inside the timed region"}
+            del rf_v, out_v
         if args.pipeline > 0 and not flush:
             # a stream of volumes: two plans, each driven by its own host thread
             # through the same host entry point, so one volume's upload overlaps

@@ -276,6 +276,25 @@ das_status das_beamform(das_plan plan, const void *rf, const float *tau_tx,
 das_status das_beamform_host(das_plan plan, const void *rf_host, const float *tau_tx_host,
                              const float *w_tx_host, void *out_host, cudaStream_t stream);
 
+/*
+ * A stream of volumes from host buffers: n_volumes records acquired with the
+ * same transmits, one after another in rf_host (n_volumes x B x Q x M x K,
+ * each in the layout of das_beamform_host), beamformed with the one tau_tx /
+ * w_tx (Q x N, host) into out_host (n_volumes x B x N), in order.  The record of
+ * volume v + 1 is copied to the device, group of transmits by group, while the
+ * kernels of volume v run: a group's copy waits only until volume v's permute
+ * has read that group's staging copy, so the host link and the kernels stay
+ * busy across volumes (the pages' streaming use, "kilohertz volume rates":
+ * ffdas docs, "How It Works").  Same arithmetic and output, bit for bit, as
+ * das_beamform_host on each volume.  Page-locked host memory is needed for the
+ * overlap.  Device buffers as das_beamform_host.
+ * Errors: as das_beamform_host, and DAS_ERR_INVALID_ARG for n_volumes < 1.
+ * Synchronous (returns when every y is in out_host).
+ */
+das_status das_beamform_host_volumes(das_plan plan, int n_volumes, const void *rf_host,
+                                     const float *tau_tx_host, const float *w_tx_host, void *out_host,
+                                     cudaStream_t stream);
+
 /* Device milliseconds of the permute and of the DAS kernel of the last
  * das_beamform on this plan, when DAS_OPT_TIMING is 1 (synchronises on the
  * recorded events).  permute_ms is 0 for the BL kernel.  Errors:

@@ -64,6 +64,7 @@ def test_host_side_rejections(libdas):
     assert libdas.das_beamform(None, None, None, None, None, None) == das.DAS_ERR_INVALID_ARG
     assert libdas.das_plan_set_option(None, 0, 0.0) == das.DAS_ERR_INVALID_ARG
     assert libdas.das_plan_launches(None, None) == das.DAS_ERR_INVALID_ARG
+    assert libdas.das_beamform_host_volumes(None, 1, None, None, None, None, None) == das.DAS_ERR_INVALID_ARG
     # unknown dtypes; the half-precision records exist for plans and das_permute only
     assert libdas.das_plan_create(ctypes.byref(h), ctypes.byref(g), rx, 1540.0, 20e6, 0.0, 1.5, 6, 1, 1, 1, 8) == das.DAS_ERR_INVALID_ARG
     one = ctypes.create_string_buffer(1024)

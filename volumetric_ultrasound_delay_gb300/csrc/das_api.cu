@@ -75,6 +75,7 @@ struct das_plan_s {
     int storage = DAS_STORAGE_NATIVE;         // DAS_OPT_STORAGE
     cudaStream_t copy_stream = nullptr;
     std::vector<cudaEvent_t> copy_ev;         // [0]: start, [1]: tau/w copied, [2+g]: group g copied
+    std::vector<cudaEvent_t> used_ev;         // [g]: the staging copy of group g read (volume streams)
     DasGeom geom{};
     DasGeom64 geom64{};
 
@@ -309,6 +310,8 @@ void release(das_plan_s *p)
     for (auto &e : p->ev)
         if (e) cudaEventDestroy(e);
     for (auto &e : p->copy_ev)
+        if (e) cudaEventDestroy(e);
+    for (auto &e : p->used_ev)
         if (e) cudaEventDestroy(e);
     if (p->done) cudaEventDestroy(p->done);
     if (p->copy_stream) cudaStreamDestroy(p->copy_stream);
@@ -817,6 +820,113 @@ das_status das_beamform_host(das_plan p, const void *rf_host, const float *tau_t
     e = cudaMemcpyAsync(out_host, p->d_out, p->out_bytes(), cudaMemcpyDeviceToHost, stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
+    return DAS_OK;
+}
+
+das_status das_beamform_host_volumes(das_plan p, int n_volumes, const void *rf_host,
+                                     const float *tau_tx_host, const float *w_tx_host, void *out_host,
+                                     cudaStream_t stream)
+{
+    if (!p) return fail(DAS_ERR_INVALID_ARG, "plan is NULL");
+    if (n_volumes < 1) return fail(DAS_ERR_INVALID_ARG, "n_volumes must be >= 1");
+    if (!rf_host || !tau_tx_host || !w_tx_host || !out_host) return fail(DAS_ERR_INVALID_ARG, "NULL buffer");
+    const int kernel = resolve_kernel(p);
+    das_status st = check_supported(p, kernel);
+    if (st != DAS_OK) return st;
+    DeviceGuard dg(p->device);
+    cudaError_t e = cudaSuccess;
+    if (!p->d_rf) e = plan_alloc(p, &p->d_rf, p->rf_bytes());
+    if (e == cudaSuccess && !p->d_out) e = plan_alloc(p, &p->d_out, p->out_bytes());
+    if (e == cudaSuccess && !p->d_tau) e = plan_alloc(p, &p->d_tau, p->txw_bytes());
+    if (e == cudaSuccess && !p->d_w) e = plan_alloc(p, &p->d_w, p->txw_bytes());
+    if (e != cudaSuccess) return cuda_fail(e, "host-path device buffers");
+    DoneMark mark{p, stream};
+    // transmit groups as das_beamform_host streams them; kernels that cannot sum
+    // transmit ranges take the record whole
+    const bool ranges = kernel == DAS_KERNEL_BRICK || kernel == DAS_KERNEL_WINDOW || kernel == DAS_KERNEL_PAIR;
+    int groups = !ranges ? 1 : (p->host_groups > 0 ? p->host_groups : (p->Q < 5 ? p->Q : 5));
+    if (groups > p->Q) groups = p->Q;
+    if (!p->copy_stream) {
+        e = cudaStreamCreateWithFlags(&p->copy_stream, cudaStreamNonBlocking);
+        if (e != cudaSuccess) { p->copy_stream = nullptr; return cuda_fail(e, "copy stream"); }
+    }
+    while ((int)p->copy_ev.size() < groups + 2) {
+        cudaEvent_t ev;
+        e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(e, "copy events");
+        p->copy_ev.push_back(ev);
+    }
+    while ((int)p->used_ev.size() < groups) {
+        cudaEvent_t ev;
+        e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(e, "copy events");
+        p->used_ev.push_back(ev);
+    }
+    const bool cplx = p->cplx32();
+    const bool half = p->half_rows();
+    const size_t eb = p->elem_bytes();
+    const size_t plane = (size_t)p->M * p->K * eb;            // one transmit of one frame
+    const size_t pitch = (size_t)p->Q * plane;                // one frame
+    // nothing queued earlier on `stream` may still read the staging buffers
+    e = cudaEventRecord(p->copy_ev[0], stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(p->copy_stream, p->copy_ev[0], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(p->d_tau, tau_tx_host, p->txw_bytes(), cudaMemcpyHostToDevice, p->copy_stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(p->d_w, w_tx_host, p->txw_bytes(), cudaMemcpyHostToDevice, p->copy_stream);
+    if (e == cudaSuccess) e = cudaEventRecord(p->copy_ev[1], p->copy_stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, p->copy_ev[1], 0);
+    if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+    if (ranges) {
+        st = ensure_scratch(p, 2, stream);
+        if (st != DAS_OK) return st;
+    }
+    unsigned *flag = kernel == DAS_KERNEL_PAIR ? p->d_flag : nullptr;
+    for (int v = 0; v < n_volumes; ++v) {
+        const char *rf_v = static_cast<const char *>(rf_host) + (size_t)v * p->rf_bytes();
+        // volume v's copy of group g waits until the kernels of volume v - 1 have
+        // read the staging copy of group g, then runs beside their later groups
+        for (int gi = 0; gi < groups && e == cudaSuccess; ++gi) {
+            const int q0 = gi * p->Q / groups, q1 = (gi + 1) * p->Q / groups;
+            if (v > 0) e = cudaStreamWaitEvent(p->copy_stream, p->used_ev[gi], 0);
+            if (e == cudaSuccess)
+                e = cudaMemcpy2DAsync(static_cast<char *>(p->d_rf) + q0 * plane, pitch, rf_v + q0 * plane, pitch,
+                                      (q1 - q0) * plane, p->B, cudaMemcpyHostToDevice, p->copy_stream);
+            if (e == cudaSuccess) e = cudaEventRecord(p->copy_ev[2 + gi], p->copy_stream);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+        if (ranges) {
+            if (flag) e = cudaMemsetAsync(flag, 0, sizeof(unsigned), stream);
+            for (int gi = 0; gi < groups && e == cudaSuccess; ++gi) {
+                const int q0 = gi * p->Q / groups, q1 = (gi + 1) * p->Q / groups;
+                e = cudaStreamWaitEvent(stream, p->copy_ev[2 + gi], 0);
+                if (e == cudaSuccess)
+                    e = das::launch_permute(p->d_rf, p->d_perm, (int)eb, p->B, p->Q, p->M, p->K, 2,
+                                            p->num_sms, stream, q0, q1, p->convert_half(), flag);
+                if (e == cudaSuccess) e = cudaEventRecord(p->used_ev[gi], stream);
+                if (e == cudaSuccess)
+                    e = kernel == DAS_KERNEL_WINDOW
+                            ? das::launch_window(p->geom, p->d_rx, p->d_perm, p->d_tau, p->d_w, p->d_out,
+                                                 stream, q0, q1, gi > 0)
+                        : kernel == DAS_KERNEL_PAIR
+                            ? das::launch_pair(p->geom, p->d_rx, p->d_perm, p->d_tau, p->d_w, p->d_out,
+                                               flag, stream, q0, q1, gi > 0)
+                            : das::launch_brick(p->geom, p->d_rx, p->d_perm, p->d_tau, p->d_w, p->d_out,
+                                                cplx, stream, q0, q1, gi > 0, half);
+            }
+            if (e != cudaSuccess) return cuda_fail(e, "streamed beamform launch");
+        } else {
+            e = cudaStreamWaitEvent(stream, p->copy_ev[2], 0);
+            if (e != cudaSuccess) return cuda_fail(e, "stream wait");
+            st = das_beamform(p, p->d_rf, p->d_tau, p->d_w, p->d_out, stream);
+            if (st != DAS_OK) return st;
+            e = cudaEventRecord(p->used_ev[0], stream);
+        }
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<char *>(out_host) + (size_t)v * p->out_bytes(), p->d_out,
+                                p->out_bytes(), cudaMemcpyDeviceToHost, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
+    }
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "synchronise");
     return DAS_OK;
 }
 

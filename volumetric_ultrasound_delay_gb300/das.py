@@ -42,6 +42,7 @@ _SIGS = {
     "das_plan_launches": (_I, [_VP, ctypes.POINTER(_I)]),
     "das_beamform": (_I, [_VP, _VP, _VP, _VP, _VP, _VP]),
     "das_beamform_host": (_I, [_VP, _VP, _VP, _VP, _VP, _VP]),
+    "das_beamform_host_volumes": (_I, [_VP, _I, _VP, _VP, _VP, _VP, _VP]),
     "das_plan_last_times": (_I, [_VP, ctypes.POINTER(_F), ctypes.POINTER(_F)]),
     "das_plan_device_bytes": (_I, [_VP, ctypes.POINTER(ctypes.c_size_t)]),
     "das_plan_destroy": (_I, [_VP]),
@@ -224,6 +225,33 @@ class Plan:
             self._h, hp(rf, "rf", self.B * self.Q * self.M * self.K),
             hp(tau_tx, "tau_tx", self.Q * self.N), hp(w_tx, "w_tx", self.Q * self.N),
             hp(out, "out", self.B * self.N), _stream_handle(stream)))
+        return out
+
+    def beamform_host_volumes(self, rf, tau_tx, w_tx, out, stream=None):
+        """A stream of V volumes from host memory: rf V x B x Q x M x K, out
+        V x B x N, one tau_tx / w_tx (Q x N) for all (copies inside, synchronous)."""
+        import torch
+        n_rec = self.B * self.Q * self.M * self.K
+        def host(a, name):
+            if isinstance(a, torch.Tensor):
+                if a.is_cuda or not a.is_contiguous():
+                    raise ValueError(f"{name} must be a contiguous host tensor")
+                return a.numel(), ctypes.c_void_p(a.data_ptr())
+            if not (isinstance(a, np.ndarray) and a.flags.c_contiguous):
+                raise ValueError(f"{name} must be a contiguous host array")
+            return a.size, a.ctypes.data_as(ctypes.c_void_p)
+        n_rf, p_rf = host(rf, "rf")
+        if n_rf % n_rec != 0 or n_rf == 0:
+            raise ValueError(f"rf must hold a whole number of {n_rec}-element records")
+        vols = n_rf // n_rec
+        n_out, p_out = host(out, "out")
+        if n_out != vols * self.B * self.N:
+            raise ValueError(f"out must hold {vols} x {self.B} x {self.N} elements")
+        n_t, p_t = host(tau_tx, "tau_tx")
+        n_w, p_w = host(w_tx, "w_tx")
+        if n_t != self.Q * self.N or n_w != self.Q * self.N:
+            raise ValueError("tau_tx and w_tx must hold Q x N elements")
+        _check(lib().das_beamform_host_volumes(self._h, vols, p_rf, p_t, p_w, p_out, _stream_handle(stream)))
         return out
 
     def last_times(self):
