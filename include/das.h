@@ -238,11 +238,13 @@ das_status das_plan_launches(das_plan plan, int *launches);
 
 /*
  * y = DAS(rf) on the device (the formula at the top of this file).
- *   rf       device, B x Q x M x K, k contiguous (float32, or interleaved
- *            complex64 for DAS_C64).
+ *   rf       device, B x Q x M x K, k contiguous, of the plan's dtype (float32,
+ *            interleaved complex64, float64, complex128, float16 or interleaved
+ *            half2).
  *   tau_tx   device, Q x N float32 transmit delays (seconds).
  *   w_tx     device, Q x N float32 transmit weights.
- *   out      device, B x N (float32 or complex64); fully overwritten.
+ *   out      device, B x N: float32 (DAS_F32, DAS_F16), complex64 (DAS_C64,
+ *            DAS_C32H), float64 or complex128; fully overwritten.
  *   stream   CUDA stream of the plan's device (0 = legacy default stream).
  * The BI, brick and window kernels first permute rf into the plan's scratch (ffdas
  * paper, Methods, batch-inner paragraph; ffdas docs, ALG2: permuted as part of
